@@ -1,0 +1,99 @@
+"""Builds the engine's CUDA library in-tree: ``_build/libfc.so``.
+
+Every ``csrc/*.cu`` file is compiled for sm_103a in parallel with nvcc and
+linked into one shared library with the CUDA runtime linked statically (the
+library then needs only the driver at run time).  No CMake, no setuptools.
+"""
+
+from __future__ import annotations
+
+import concurrent.futures as cf
+import glob
+import os
+import shutil
+import subprocess
+import sys
+
+HERE = os.path.dirname(os.path.abspath(__file__))
+ROOT = os.path.dirname(HERE)
+CSRC = os.path.join(HERE, "csrc")
+INCLUDE = os.path.join(ROOT, "include")
+OUT_DIR = os.path.join(HERE, "_build")
+LIB_NAME = "libfc.so"
+LIB_PATH = os.path.join(OUT_DIR, LIB_NAME)
+
+ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
+NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC",
+              "-Xcompiler", "-fvisibility=hidden", "--expt-relaxed-constexpr"]
+
+
+def _nvcc() -> str:
+    path = shutil.which("nvcc")
+    if path:
+        return path
+    cand = "/usr/local/cuda/bin/nvcc"
+    if os.path.exists(cand):
+        return cand
+    raise RuntimeError("nvcc not found: the CUDA toolkit is required to build libfc")
+
+
+def _sources():
+    return sorted(glob.glob(os.path.join(CSRC, "*.cu")))
+
+
+def _headers():
+    return (sorted(glob.glob(os.path.join(CSRC, "*.cuh")))
+            + sorted(glob.glob(os.path.join(CSRC, "*.h")))
+            + [os.path.join(INCLUDE, "fc.h")])
+
+
+def _stale(target: str, deps) -> bool:
+    if not os.path.exists(target):
+        return True
+    t = os.path.getmtime(target)
+    return any(os.path.getmtime(d) > t for d in deps)
+
+
+def build_library(force: bool = False, verbose: bool = False) -> str:
+    """Compile (if needed) and return the path of libfc.so."""
+    os.makedirs(OUT_DIR, exist_ok=True)
+    srcs = _sources()
+    hdrs = _headers()
+    if not force and not _stale(LIB_PATH, srcs + hdrs + [__file__]):
+        return LIB_PATH
+    nvcc = _nvcc()
+    objs = []
+    jobs = []
+    for src in srcs:
+        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        objs.append(obj)
+        cmd = [nvcc, *ARCH, *NVCC_FLAGS, "-I", INCLUDE, "-I", CSRC,
+               "-c", src, "-o", obj]
+        if verbose:
+            cmd.insert(1, "-Xptxas=-v")
+        jobs.append(cmd)
+
+    def run(cmd):
+        p = subprocess.run(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT,
+                           text=True)
+        return cmd, p.returncode, p.stdout
+
+    with cf.ThreadPoolExecutor(max_workers=max(1, min(len(jobs), os.cpu_count() or 4))) as ex:
+        results = list(ex.map(run, jobs))
+    for cmd, rc, out in results:
+        if verbose or rc != 0:
+            sys.stderr.write(out)
+        if rc != 0:
+            raise RuntimeError("nvcc failed: " + " ".join(cmd))
+    tmp = LIB_PATH + ".tmp.%d" % os.getpid()
+    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    p = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+    if p.returncode != 0:
+        sys.stderr.write(p.stdout)
+        raise RuntimeError("link failed: " + " ".join(link))
+    os.replace(tmp, LIB_PATH)
+    return LIB_PATH
+
+
+if __name__ == "__main__":
+    print(build_library(force="--force" in sys.argv, verbose="-v" in sys.argv))

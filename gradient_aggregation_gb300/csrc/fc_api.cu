@@ -1,0 +1,458 @@
+// The C ABI of libfc: argument checks, layout/tiling arithmetic on the host,
+// and kernel launches.  Declarations and the contract of every entry point
+// are in include/fc.h.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include "fc.h"
+#include "fc_internal.h"
+
+using namespace fc;
+
+namespace {
+
+thread_local char g_err[512] = "";
+
+fc_status fail(fc_status st, const char *fmt, ...)
+{
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_err, sizeof(g_err), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+fc_status ok()
+{
+    g_err[0] = '\0';
+    return FC_OK;
+}
+
+fc_status cuda_fail(cudaError_t e, const char *what)
+{
+    return fail(FC_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e),
+                cudaGetErrorString(e));
+}
+
+bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
+
+// Makes the device that owns `stream` (or `ptr` for the NULL stream) current.
+fc_status bind_device(void *stream, const void *ptr)
+{
+    (void)cudaGetLastError();  // clear a stale error of this runtime
+    int dev = -1;
+    cudaError_t e;
+    if (stream) {
+        e = cudaStreamGetDevice((cudaStream_t)stream, &dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetDevice");
+    } else {
+        cudaPointerAttributes at;
+        e = cudaPointerGetAttributes(&at, ptr);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+        if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+            return fail(FC_ERR_INVALID_ARG, "pointer %p is not device memory", ptr);
+        dev = at.device;
+    }
+    int cur = -1;
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (cur != dev) {
+        e = cudaSetDevice(dev);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+    }
+    return FC_OK;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+TileGeom geom(int64_t N, int64_t cs)
+{
+    TileGeom G;
+    G.N = N;
+    G.cs = cs;
+    G.P = ceil_div(cs, FC_TILE);
+    return G;
+}
+
+size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+
+size_t ws_partials_bytes(int64_t C, int64_t P) { return align256((size_t)(C * P) * sizeof(double)); }
+
+fc_status check_sizes(int32_t L, const int64_t *sizes, int64_t *N_out)
+{
+    if (L < 1) return fail(FC_ERR_INVALID_ARG, "L = %d must be >= 1", L);
+    if (!sizes) return fail(FC_ERR_INVALID_ARG, "sizes is NULL");
+    int64_t N = 0;
+    for (int32_t l = 0; l < L; ++l) {
+        if (sizes[l] < 0) return fail(FC_ERR_INVALID_ARG, "sizes[%d] = %lld < 0", l, (long long)sizes[l]);
+        if (sizes[l] > ((int64_t)1 << 48) || N > ((int64_t)1 << 48))
+            return fail(FC_ERR_INVALID_ARG, "sizes too large");
+        N += sizes[l];
+    }
+    if (N < 1) return fail(FC_ERR_INVALID_ARG, "the sizes sum to 0");
+    *N_out = N;
+    return FC_OK;
+}
+
+fc_status check_table(const void *const *grads, int32_t W, int32_t L,
+                      const int64_t *sizes)
+{
+    if (!grads) return fail(FC_ERR_INVALID_ARG, "grads is NULL");
+    if (W < 1) return fail(FC_ERR_INVALID_ARG, "W = %d must be >= 1", W);
+    if (L > FC_MAX_TABLE_LAYERS)
+        return fail(FC_ERR_LIMIT, "L = %d exceeds FC_MAX_TABLE_LAYERS = %d", L, FC_MAX_TABLE_LAYERS);
+    if ((int64_t)W * L > FC_MAX_TABLE_PTRS)
+        return fail(FC_ERR_LIMIT, "W*L = %lld exceeds FC_MAX_TABLE_PTRS = %d",
+                    (long long)W * L, FC_MAX_TABLE_PTRS);
+    for (int64_t i = 0; i < (int64_t)W * L; ++i) {
+        if (sizes[i % L] == 0) continue;
+        if (!grads[i]) return fail(FC_ERR_INVALID_ARG, "grads[%lld] is NULL", (long long)i);
+        if (!aligned(grads[i], 2))
+            return fail(FC_ERR_ALIGNMENT, "grads[%lld] is not 2-byte aligned", (long long)i);
+    }
+    return FC_OK;
+}
+
+bool fits_small(int32_t W, int32_t L)
+{
+    return L <= 64 && (int64_t)W * L <= 256;
+}
+
+const void *first_nonnull(const void *const *grads, int64_t n)
+{
+    for (int64_t i = 0; i < n; ++i)
+        if (grads[i]) return grads[i];
+    return nullptr;
+}
+
+fc_status check_f32(const void *p, const char *name, bool may_be_null)
+{
+    if (!p) return may_be_null ? FC_OK : fail(FC_ERR_INVALID_ARG, "%s is NULL", name);
+    if (!aligned(p, 16)) return fail(FC_ERR_ALIGNMENT, "%s is not 16-byte aligned", name);
+    return FC_OK;
+}
+
+#define TRY(x)                         \
+    do {                               \
+        fc_status _st = (x);           \
+        if (_st != FC_OK) return _st;  \
+    } while (0)
+
+}  // namespace
+
+extern "C" {
+
+const char *fc_last_error(void) { return g_err; }
+
+int32_t fc_version(void) { return 100; }
+
+int64_t fc_num_chunks(int64_t N, int64_t chunk)
+{
+    if (N < 0 || chunk < 1) return -1;
+    return ceil_div(N, chunk);
+}
+
+int64_t fc_keep_count(int64_t C, int64_t keep_num, int64_t keep_den)
+{
+    if (C < 1 || keep_num < 0 || keep_den < 1) return -1;
+    if (keep_num > keep_den) keep_num = keep_den;
+    int64_t k = ceil_div(C * keep_num, keep_den);
+    if (k < 1) k = 1;
+    if (k > C) k = C;
+    return k;
+}
+
+fc_status fc_layout(int32_t L, const int64_t *sizes, int64_t *offsets,
+                    int64_t *N_out)
+{
+    int64_t N = 0;
+    TRY(check_sizes(L, sizes, &N));
+    if (offsets) {
+        int64_t acc = 0;
+        for (int32_t l = 0; l < L; ++l) {
+            offsets[l] = acc;
+            acc += sizes[l];
+        }
+    }
+    if (N_out) *N_out = N;
+    return ok();
+}
+
+fc_status fc_fuse_pack(const void *const *grads, int32_t W, int32_t L,
+                       const int64_t *sizes, int64_t *offsets, void *fused,
+                       void *stream)
+{
+    int64_t N = 0;
+    TRY(check_sizes(L, sizes, &N));
+    TRY(check_table(grads, W, L, sizes));
+    if (!fused) return fail(FC_ERR_INVALID_ARG, "fused is NULL");
+    if (!aligned(fused, 16)) return fail(FC_ERR_ALIGNMENT, "fused is not 16-byte aligned");
+    if (offsets) TRY(fc_layout(L, sizes, offsets, nullptr));
+    TRY(bind_device(stream, fused));
+    cudaError_t e;
+    if (fits_small(W, L)) {
+        TableS tab;
+        fill_table(tab, grads, W, L, sizes);
+        e = launch_pack(tab, N, (__half *)fused, (cudaStream_t)stream);
+    } else {
+        static thread_local TableL tab;
+        fill_table(tab, grads, W, L, sizes);
+        e = launch_pack(tab, N, (__half *)fused, (cudaStream_t)stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "fuse_pack launch");
+    return ok();
+}
+
+fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
+                         float loss_scale, const float *residual_in,
+                         float *out, void *stream)
+{
+    if (!fused) return fail(FC_ERR_INVALID_ARG, "fused is NULL");
+    if (W < 1 || W > FC_MAX_TABLE_PTRS)
+        return fail(FC_ERR_INVALID_ARG, "W = %d out of [1, %d]", W, FC_MAX_TABLE_PTRS);
+    if (N < 1) return fail(FC_ERR_INVALID_ARG, "N = %lld must be >= 1", (long long)N);
+    if (!(loss_scale > 0.f) || !isfinite(loss_scale))
+        return fail(FC_ERR_INVALID_ARG, "loss_scale must be finite and > 0");
+    if (!aligned(fused, 2)) return fail(FC_ERR_ALIGNMENT, "fused is not 2-byte aligned");
+    TRY(check_f32(residual_in, "residual_in", true));
+    TRY(check_f32(out, "out", false));
+    TRY(bind_device(stream, out));
+    const float u = (float)(1.0 / ((double)loss_scale * (double)W));
+    const TileGeom G = geom(N, FC_TILE);
+    const int64_t tiles = ceil_div(N, FC_TILE);
+    const int64_t sizes[1] = {N};
+    cudaError_t e;
+    // one "layer" per worker: row w of the fused buffer
+    if (W <= 256) {
+        TableS tab;
+        const void *rows[256];
+        for (int w = 0; w < W; ++w) rows[w] = (const __half *)fused + (int64_t)w * N;
+        fill_table(tab, rows, W, 1, sizes);
+        e = launch_reduce(tab, G, tiles, u, residual_in, out, nullptr, (cudaStream_t)stream);
+    } else {
+        static thread_local TableL tab;
+        static thread_local const void *rows[FC_MAX_TABLE_PTRS];
+        for (int w = 0; w < W; ++w) rows[w] = (const __half *)fused + (int64_t)w * N;
+        fill_table(tab, rows, W, 1, sizes);
+        e = launch_reduce(tab, G, tiles, u, residual_in, out, nullptr, (cudaStream_t)stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "tree_reduce launch");
+    return ok();
+}
+
+fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
+                         float *norms, void *stream)
+{
+    if (N < 1) return fail(FC_ERR_INVALID_ARG, "N must be >= 1");
+    if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
+    TRY(check_f32(a, "a", false));
+    TRY(check_f32(norms, "norms", false));
+    TRY(bind_device(stream, a));
+    const int64_t C = ceil_div(N, chunk);
+    cudaError_t e = launch_norms(a, geom(N, chunk), C, norms, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "chunk_norms launch");
+    return ok();
+}
+
+static fc_status check_select_args(int64_t C, int64_t k, const int32_t *idx,
+                                   const uint8_t *mask, const float *threshold)
+{
+    if (C < 1 || C > 0x7fffffffLL) return fail(FC_ERR_INVALID_ARG, "C = %lld out of range", (long long)C);
+    if (k < 1 || k > C) return fail(FC_ERR_INVALID_ARG, "k = %lld must be in [1, C = %lld]", (long long)k, (long long)C);
+    if (!idx) return fail(FC_ERR_INVALID_ARG, "idx is NULL");
+    if (!mask) return fail(FC_ERR_INVALID_ARG, "mask is NULL");
+    if (!threshold) return fail(FC_ERR_INVALID_ARG, "threshold is NULL");
+    if (!aligned(idx, 4) || !aligned(threshold, 4))
+        return fail(FC_ERR_ALIGNMENT, "idx/threshold are not 4-byte aligned");
+    return FC_OK;
+}
+
+fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
+                          const float *a, int64_t N, int64_t chunk,
+                          int32_t *idx, uint8_t *mask, float *packed,
+                          float *threshold, void *stream)
+{
+    TRY(check_select_args(C, k, idx, mask, threshold));
+    TRY(check_f32(norms, "norms", false));
+    if (packed) {
+        TRY(check_f32(a, "a", false));
+        TRY(check_f32(packed, "packed", false));
+        if (chunk < 1 || N < 1 || ceil_div(N, chunk) != C)
+            return fail(FC_ERR_INVALID_ARG, "N and chunk do not give C chunks");
+    }
+    TRY(bind_device(stream, norms));
+    cudaError_t e = launch_select(nullptr, 1, const_cast<float *>(norms), C, k,
+                                  idx, mask, nullptr, threshold, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "chunk_select launch");
+    if (packed) {
+        e = launch_gather(a, N, chunk, ceil_div(chunk, FC_TILE), idx, k, packed,
+                          (cudaStream_t)stream);
+        if (e != cudaSuccess) return cuda_fail(e, "gather launch");
+    }
+    return ok();
+}
+
+static fc_status check_update_args(const float *a, const uint8_t *mask,
+                                   int64_t N, int64_t chunk, float lr,
+                                   float momentum, float *residual,
+                                   float *velocity, float *weights,
+                                   void *weights_fp16)
+{
+    if (N < 1) return fail(FC_ERR_INVALID_ARG, "N must be >= 1");
+    if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
+    if (!isfinite(lr) || !isfinite(momentum))
+        return fail(FC_ERR_INVALID_ARG, "lr and momentum must be finite");
+    if (!mask) return fail(FC_ERR_INVALID_ARG, "mask is NULL");
+    TRY(check_f32(a, "a", false));
+    TRY(check_f32(residual, "residual", false));
+    TRY(check_f32(velocity, "velocity", false));
+    TRY(check_f32(weights, "weights", false));
+    TRY(check_f32(weights_fp16, "weights_fp16", true));
+    return FC_OK;
+}
+
+fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
+                                 int64_t N, int64_t chunk, float lr,
+                                 float momentum, float *residual,
+                                 float *velocity, float *weights,
+                                 void *weights_fp16, void *stream)
+{
+    TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
+                          weights, weights_fp16));
+    TRY(bind_device(stream, a));
+    const TileGeom G = geom(N, chunk);
+    const int64_t tiles = ceil_div(N, chunk) * G.P;
+    cudaError_t e = launch_update(G, tiles, a, mask, nullptr, nullptr, lr,
+                                  momentum, residual, velocity, weights,
+                                  (__half *)weights_fp16, a == residual,
+                                  (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "update launch");
+    return ok();
+}
+
+size_t fc_step_workspace_size(int64_t N, int64_t chunk)
+{
+    if (N < 1 || chunk < 1) return 0;
+    const int64_t C = ceil_div(N, chunk);
+    const int64_t P = ceil_div(chunk, FC_TILE);
+    return ws_partials_bytes(C, P) + align256((size_t)C * sizeof(int32_t));
+}
+
+static fc_status check_ws(int64_t N, int64_t chunk, void *ws, size_t bytes)
+{
+    if (!ws) return fail(FC_ERR_WORKSPACE, "workspace is NULL");
+    if (!aligned(ws, 256)) return fail(FC_ERR_ALIGNMENT, "workspace is not 256-byte aligned");
+    const size_t need = fc_step_workspace_size(N, chunk);
+    if (bytes < need)
+        return fail(FC_ERR_WORKSPACE, "workspace has %zu bytes, %zu needed", bytes, need);
+    return FC_OK;
+}
+
+fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
+                         const int64_t *sizes, float loss_scale,
+                         int64_t chunk, const float *residual, float *a,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    int64_t N = 0;
+    TRY(check_sizes(L, sizes, &N));
+    TRY(check_table(grads, W, L, sizes));
+    if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
+    if (!(loss_scale > 0.f) || !isfinite(loss_scale))
+        return fail(FC_ERR_INVALID_ARG, "loss_scale must be finite and > 0");
+    TRY(check_f32(residual, "residual", true));
+    TRY(check_f32(a, "a", false));
+    TRY(check_ws(N, chunk, workspace, workspace_bytes));
+    TRY(bind_device(stream, a));
+    const float u = (float)(1.0 / ((double)loss_scale * (double)W));
+    const TileGeom G = geom(N, chunk);
+    const int64_t tiles = ceil_div(N, chunk) * G.P;
+    double *partials = (double *)workspace;
+    cudaError_t e;
+    if (fits_small(W, L)) {
+        TableS tab;
+        fill_table(tab, grads, W, L, sizes);
+        e = launch_reduce(tab, G, tiles, u, residual, a, partials, (cudaStream_t)stream);
+    } else {
+        static thread_local TableL tab;
+        fill_table(tab, grads, W, L, sizes);
+        e = launch_reduce(tab, G, tiles, u, residual, a, partials, (cudaStream_t)stream);
+    }
+    if (e != cudaSuccess) return cuda_fail(e, "step_reduce launch");
+    return ok();
+}
+
+fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
+                         int32_t *idx, uint8_t *mask, float *threshold,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    if (N < 1 || chunk < 1) return fail(FC_ERR_INVALID_ARG, "N and chunk must be >= 1");
+    const int64_t C = ceil_div(N, chunk);
+    TRY(check_select_args(C, k, idx, mask, threshold));
+    TRY(check_f32(norms, "norms", false));
+    TRY(check_ws(N, chunk, workspace, workspace_bytes));
+    TRY(bind_device(stream, norms));
+    const int64_t P = ceil_div(chunk, FC_TILE);
+    double *partials = (double *)workspace;
+    int32_t *slot = (int32_t *)((char *)workspace + ws_partials_bytes(C, P));
+    cudaError_t e = launch_select(partials, P, norms, C, k, idx, mask, slot,
+                                  threshold, (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "step_select launch");
+    return ok();
+}
+
+fc_status fc_step_update(const float *a, int64_t N, int64_t chunk, float lr,
+                         float momentum, float *residual, float *velocity,
+                         float *weights, void *weights_fp16,
+                         const uint8_t *mask, float *packed, void *workspace,
+                         size_t workspace_bytes, void *stream)
+{
+    TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
+                          weights, weights_fp16));
+    TRY(check_f32(packed, "packed", true));
+    TRY(check_ws(N, chunk, workspace, workspace_bytes));
+    TRY(bind_device(stream, a));
+    const TileGeom G = geom(N, chunk);
+    const int64_t C = ceil_div(N, chunk);
+    const int32_t *slot = (const int32_t *)((char *)workspace + ws_partials_bytes(C, G.P));
+    cudaError_t e = launch_update(G, C * G.P, a, mask, slot, packed, lr,
+                                  momentum, residual, velocity, weights,
+                                  (__half *)weights_fp16, a == residual,
+                                  (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "step_update launch");
+    return ok();
+}
+
+fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
+                  const int64_t *sizes, float loss_scale, int64_t chunk,
+                  int64_t k, float lr, float momentum, float *residual,
+                  float *a, float *velocity, float *weights,
+                  void *weights_fp16, float *norms, int32_t *idx,
+                  uint8_t *mask, float *packed, float *threshold,
+                  void *workspace, size_t workspace_bytes, void *stream)
+{
+    int64_t N = 0;
+    TRY(check_sizes(L, sizes, &N));
+    // check everything before the first launch so that an error launches
+    // nothing
+    TRY(check_table(grads, W, L, sizes));
+    if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
+    TRY(check_select_args(ceil_div(N, chunk), k, idx, mask, threshold));
+    TRY(check_f32(norms, "norms", false));
+    TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
+                          weights, weights_fp16));
+    TRY(check_f32(packed, "packed", true));
+    TRY(fc_step_reduce(grads, W, L, sizes, loss_scale, chunk, residual, a,
+                       workspace, workspace_bytes, stream));
+    TRY(fc_step_select(N, chunk, k, norms, idx, mask, threshold, workspace,
+                       workspace_bytes, stream));
+    TRY(fc_step_update(a, N, chunk, lr, momentum, residual, velocity, weights,
+                       weights_fp16, mask, packed, workspace, workspace_bytes,
+                       stream));
+    return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,240 @@
+// Device-side building blocks shared by the engine's kernels.
+//
+// Layout conventions (all kernels):
+//  * The fused vector has N elements; layer l occupies [off[l], off[l+1]).
+//  * Chunks of `cs` elements split the fused vector (the last may be short).
+//  * Work is cut into tiles of at most FC_TILE elements that never straddle a
+//    chunk: chunk c owns tiles c*P .. c*P+P-1 with P = ceil(cs / FC_TILE);
+//    tile j of chunk c covers [c*cs + j*FC_TILE, min(+FC_TILE, c*cs+cs, N)).
+//  * Inside a tile, thread t of a 256-thread block handles the 8-element
+//    groups [8g, 8g+8) (absolute fused index, clipped to the tile) with
+//    g = floor(lo/8) + t + 256*r.  The sum of squares of a tile is formed the
+//    same way by every kernel that needs it, so the norms are bitwise
+//    reproducible across the pipeline and the standalone calls.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#define FC_TILE 2048
+#define FC_BLOCK 256
+#define FC_GROUP 8
+
+namespace fc {
+
+// Worker x layer pointer table, passed by value as a __grid_constant__
+// kernel parameter (read from the constant bank, never copied).
+template <int MAXP, int MAXL>
+struct Table {
+    int32_t W, L;
+    int64_t off[MAXL + 1];               // fused offsets, off[L] = N
+    uint32_t vec[(MAXL + 31) / 32];      // bit l: every worker's layer l is
+                                         // 16-byte aligned at fused index 0 mod 8
+    const __half *ptr[MAXP];             // ptr[w*L + l]
+};
+using TableS = Table<256, 64>;
+using TableL = Table<3072, 512>;
+
+struct TileGeom {
+    int64_t N;   // elements
+    int64_t cs;  // chunk size
+    int64_t P;   // tiles per chunk
+};
+
+__device__ __forceinline__ bool tile_range(const TileGeom &G, int64_t t,
+                                           int64_t &lo, int64_t &hi,
+                                           int64_t &c, int64_t &hi_nominal)
+{
+    c = t / G.P;
+    int64_t j = t - c * G.P;
+    int64_t cend = c * G.cs + G.cs;
+    lo = c * G.cs + j * FC_TILE;
+    hi_nominal = lo + FC_TILE < cend ? lo + FC_TILE : cend;
+    hi = hi_nominal < G.N ? hi_nominal : G.N;
+    return lo < hi;
+}
+
+// Smallest l with off[l+1] > f (skips empty layers).
+template <class Tab>
+__device__ __forceinline__ int find_layer(const Tab &t, int64_t f)
+{
+    int lo = 0, hi = t.L - 1;
+    while (lo < hi) {
+        int mid = (lo + hi) >> 1;
+        if (t.off[mid + 1] > f)
+            hi = mid;
+        else
+            lo = mid + 1;
+    }
+    return lo;
+}
+
+// ---- cache-hinted memory access ---------------------------------------------
+
+__device__ __forceinline__ uint64_t policy_evict_first()
+{
+    uint64_t p;
+    asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 16-byte streaming load of read-only data (the worker gradients).
+__device__ __forceinline__ uint4 ld_stream16(const void *ptr, uint64_t pol)
+{
+    uint4 v;
+    asm("ld.global.nc.L1::no_allocate.L2::cache_hint.v4.u32 {%0,%1,%2,%3}, [%4], %5;"
+        : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+        : "l"(ptr), "l"(pol));
+    return v;
+}
+
+__device__ __forceinline__ float ld_half_as_float(const __half *p)
+{
+    unsigned short b = __ldg(reinterpret_cast<const unsigned short *>(p));
+    return __half2float(__ushort_as_half(b));
+}
+
+__device__ __forceinline__ void unpack8(const uint4 &q, float (&x)[8])
+{
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = *reinterpret_cast<const __half2 *>(&w[i]);
+        float2 f = __half22float2(h);
+        x[2 * i] = f.x;
+        x[2 * i + 1] = f.y;
+    }
+}
+
+// ---- the binary reduction tree over the workers ------------------------------
+//
+// Level-order adjacent pairing with an odd element carried up equals the
+// binary-counter form used here: complete subtrees of 2^h leaves are merged
+// into slot h as they arrive (older partial on the left), and the leftover
+// slots are folded from the lowest height up at the end.  Leaves arrive in
+// batches of 8 (one subtree of height 3) so that eight 16-byte loads are in
+// flight at once; the W % 8 remainder arrives as subtrees of 4, 2 and 1.
+
+template <int H0, int MAXH, int V>
+__device__ __forceinline__ void tree_push(float (&acc)[MAXH][V], int cnt,
+                                          float (&x)[V])
+{
+    bool carry = true;
+#pragma unroll
+    for (int h = H0; h < MAXH; ++h) {
+        if (carry) {
+            if ((cnt >> h) & 1) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) x[e] = __fadd_rn(acc[h][e], x[e]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) acc[h][e] = x[e];
+                carry = false;
+            }
+        }
+    }
+}
+
+// Load(w, float (&x)[V]) fills the V values of worker w.
+template <int WT, int MAXH, int V, class Load>
+__device__ __forceinline__ void tree_sum(int Wrt, Load &&load, float (&out)[V])
+{
+    const int W = WT > 0 ? WT : Wrt;
+    float acc[MAXH][V];
+    int done = 0;
+#pragma unroll
+    for (; done + 8 <= W; done += 8) {
+        float x[8][V];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) load(done + u, x[u]);
+#pragma unroll
+        for (int e = 0; e < V; ++e) {
+            float p0 = __fadd_rn(x[0][e], x[1][e]);
+            float p1 = __fadd_rn(x[2][e], x[3][e]);
+            float p2 = __fadd_rn(x[4][e], x[5][e]);
+            float p3 = __fadd_rn(x[6][e], x[7][e]);
+            x[0][e] = __fadd_rn(__fadd_rn(p0, p1), __fadd_rn(p2, p3));
+        }
+        tree_push<3>(acc, done, x[0]);
+    }
+    if (W - done >= 4) {
+        float x[4][V];
+#pragma unroll
+        for (int u = 0; u < 4; ++u) load(done + u, x[u]);
+#pragma unroll
+        for (int e = 0; e < V; ++e)
+            x[0][e] = __fadd_rn(__fadd_rn(x[0][e], x[1][e]),
+                                __fadd_rn(x[2][e], x[3][e]));
+        tree_push<2>(acc, done, x[0]);
+        done += 4;
+    }
+    if (W - done >= 2) {
+        float x[2][V];
+        load(done, x[0]);
+        load(done + 1, x[1]);
+#pragma unroll
+        for (int e = 0; e < V; ++e) x[0][e] = __fadd_rn(x[0][e], x[1][e]);
+        tree_push<1>(acc, done, x[0]);
+        done += 2;
+    }
+    if (W - done >= 1) {
+        float x[V];
+        load(done, x);
+        tree_push<0>(acc, done, x);
+        done += 1;
+    }
+    bool have = false;
+#pragma unroll
+    for (int h = 0; h < MAXH; ++h) {
+        if ((W >> h) & 1) {
+            if (!have) {
+#pragma unroll
+                for (int e = 0; e < V; ++e) out[e] = acc[h][e];
+                have = true;
+            } else {
+#pragma unroll
+                for (int e = 0; e < V; ++e) out[e] = __fadd_rn(acc[h][e], out[e]);
+            }
+        }
+    }
+}
+
+// ---- sums of squares ------------------------------------------------------------
+
+// Pairwise sum of squares of 8 values; v[e] must be 0 for masked elements.
+__device__ __forceinline__ float group_sumsq(const float (&v)[8])
+{
+    float q[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) q[e] = __fmul_rn(v[e], v[e]);
+    return __fadd_rn(__fadd_rn(__fadd_rn(q[0], q[1]), __fadd_rn(q[2], q[3])),
+                     __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
+}
+
+// Tile total of the per-thread sums: butterfly within each warp (every lane
+// ends with the same value), then the 8 warp sums added in order in fp64.
+// Must be called by all FC_BLOCK threads; the result is valid in thread 0.
+__device__ __forceinline__ double block_tile_sumsq(float tss, float *red8)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        tss = __fadd_rn(tss, __shfl_xor_sync(0xffffffffu, tss, o));
+    const int warp = threadIdx.x >> 5;
+    __syncthreads();  // red8 may still be read from the previous tile
+    if ((threadIdx.x & 31) == 0) red8[warp] = tss;
+    __syncthreads();
+    double d = 0.0;
+    if (threadIdx.x == 0) {
+#pragma unroll
+        for (int w = 0; w < FC_BLOCK / 32; ++w) d = __dadd_rn(d, (double)red8[w]);
+    }
+    return d;
+}
+
+__device__ __forceinline__ float norm_from_sumsq(double ss)
+{
+    return __double2float_rn(__dsqrt_rn(ss));
+}
+
+}  // namespace fc

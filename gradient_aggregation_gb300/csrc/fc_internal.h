@@ -1,0 +1,48 @@
+// Launchers shared between the engine's translation units (not exported).
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "fc_common.cuh"
+
+namespace fc {
+
+// Builds a table; returns false if it does not fit the given tier.
+template <class Tab>
+bool fill_table(Tab &t, const void *const *grads, int32_t W, int32_t L,
+                const int64_t *sizes);
+
+// Phase-1 / fc_tree_reduce kernel launch.  `partials` may be NULL.
+template <class Tab>
+cudaError_t launch_reduce(const Tab &tab, const TileGeom &G, int64_t tiles,
+                          float u, const float *resid, float *out,
+                          double *partials, cudaStream_t s);
+
+template <class Tab>
+cudaError_t launch_pack(const Tab &tab, int64_t N, __half *fused,
+                        cudaStream_t s);
+
+cudaError_t launch_norms(const float *a, const TileGeom &G, int64_t C,
+                         float *norms, cudaStream_t s);
+
+// partials == NULL: norms are an input.  Otherwise norms are written from
+// the partials first.  slot may be NULL.
+cudaError_t launch_select(const double *partials, int64_t P, float *norms,
+                          int64_t C, int64_t k, int32_t *idx, uint8_t *mask,
+                          int32_t *slot, float *threshold, cudaStream_t s);
+
+cudaError_t launch_gather(const float *a, int64_t N, int64_t cs, int64_t P,
+                          const int32_t *idx, int64_t k, float *packed,
+                          cudaStream_t s);
+
+cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
+                          const uint8_t *mask, const int32_t *slot,
+                          float *packed, float lr, float mu, float *r,
+                          float *v, float *w, __half *w16, bool inplace,
+                          cudaStream_t s);
+
+// Blocks to launch for a grid-stride kernel: min(work, SMs * resident).
+int grid_for(const void *kernel, int block, size_t smem, int64_t work);
+
+}  // namespace fc

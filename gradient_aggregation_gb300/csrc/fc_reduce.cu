@@ -1,0 +1,192 @@
+// a1 + a2 (+ the partial sums of a3): fuse and tree-reduce the workers'
+// gradients.
+//
+// FireCaffe (arXiv 1511.00175), §6: the workers' gradient vectors are summed
+// element-wise, through a reduction tree of branching factor 2 and depth
+// log2(p).  GradientFlow (arXiv 1902.06855), abstract: mixed precision
+// (fp16 gradients, fp32 sums here) and lazy allreduce, which fuses the
+// per-layer operations into one; here the fusion is a layout (offsets) that
+// the reduction reads through, so the fused copy need not be materialised.
+//
+// GB300 mapping: one pass over HBM, each element of each worker read exactly
+// once with 16-byte streaming loads (L1 bypass, L2 evict-first); eight
+// workers' loads in flight per thread before their subtree is formed in
+// registers; fp32 results written once; the chunk sums of squares formed from
+// the registers, so the norms cost no extra pass.
+#include <stdio.h>
+
+#include "fc_internal.h"
+
+namespace fc {
+
+template <class Tab>
+bool fill_table(Tab &t, const void *const *grads, int32_t W, int32_t L,
+                const int64_t *sizes)
+{
+    const int maxp = (int)(sizeof(t.ptr) / sizeof(t.ptr[0]));
+    const int maxl = (int)(sizeof(t.off) / sizeof(t.off[0])) - 1;
+    if (L > maxl || (int64_t)W * L > maxp) return false;
+    t.W = W;
+    t.L = L;
+    int64_t acc = 0;
+    for (int l = 0; l < L; ++l) {
+        t.off[l] = acc;
+        acc += sizes[l];
+    }
+    t.off[L] = acc;
+    for (int i = 0; i < (maxl + 31) / 32; ++i) t.vec[i] = 0;
+    for (int l = 0; l < L; ++l) {
+        bool ok = true;
+        for (int w = 0; w < W; ++w) {
+            uintptr_t p = (uintptr_t)grads[(int64_t)w * L + l];
+            if ((p - 2u * (uintptr_t)t.off[l]) & 15u) ok = false;
+        }
+        if (ok) t.vec[l >> 5] |= 1u << (l & 31);
+    }
+    for (int64_t i = 0; i < (int64_t)W * L; ++i)
+        t.ptr[i] = static_cast<const __half *>(grads[i]);
+    return true;
+}
+
+template bool fill_table<TableS>(TableS &, const void *const *, int32_t,
+                                 int32_t, const int64_t *);
+template bool fill_table<TableL>(TableL &, const void *const *, int32_t,
+                                 int32_t, const int64_t *);
+
+int grid_for(const void *kernel, int block, size_t smem, int64_t work)
+{
+    int dev = 0, sms = 0, per_sm = 0;
+    cudaGetDevice(&dev);
+    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block,
+                                                      smem) != cudaSuccess ||
+        per_sm < 1)
+        per_sm = 1;
+    if (sms < 1) sms = 1;
+    int64_t g = (int64_t)sms * per_sm;
+    if (work < g) g = work;
+    return g < 1 ? 1 : (int)g;
+}
+
+// ---- a2 kernel ------------------------------------------------------------------
+
+template <class Tab, int WT, int MAXH>
+__global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : 2)
+    k_reduce(const __grid_constant__ Tab tab, const TileGeom G,
+             const int64_t tiles, const float u, const float *resid,
+             float *out, double *partials)
+{
+    __shared__ float red8[FC_BLOCK / 32];
+    const uint64_t pol = policy_evict_first();
+    const int W = WT > 0 ? WT : tab.W;
+    const int L = tab.L;
+
+    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
+        int64_t lo, hi, c, hin;
+        const bool any = tile_range(G, t, lo, hi, c, hin);
+        float tss = 0.f;
+        if (any) {
+            const int64_t g1 = (hi + 7) >> 3;
+            for (int64_t g = (lo >> 3) + threadIdx.x; g < g1; g += FC_BLOCK) {
+                const int64_t f0 = g << 3;
+                float a[8];
+                const bool full = (f0 >= lo) && (f0 + 8 <= hi);
+                int l = find_layer(tab, f0 > lo ? f0 : lo);
+                if (full && f0 + 8 <= tab.off[l + 1] &&
+                    ((tab.vec[l >> 5] >> (l & 31)) & 1u)) {
+                    // vector path: 8 consecutive elements of one layer
+                    const int64_t j = f0 - tab.off[l];
+                    tree_sum<WT, MAXH, 8>(
+                        W,
+                        [&](int w, float(&x)[8]) {
+                            unpack8(ld_stream16(tab.ptr[w * L + l] + j, pol), x);
+                        },
+                        a);
+                    float r[8];
+                    if (resid) {
+                        const float4 r0 = __ldcs(reinterpret_cast<const float4 *>(resid + f0));
+                        const float4 r1 = __ldcs(reinterpret_cast<const float4 *>(resid + f0 + 4));
+                        r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
+                        r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        a[e] = __fmul_rn(a[e], u);
+                        if (resid) a[e] = __fadd_rn(a[e], r[e]);
+                    }
+                    reinterpret_cast<float4 *>(out + f0)[0] = make_float4(a[0], a[1], a[2], a[3]);
+                    reinterpret_cast<float4 *>(out + f0)[1] = make_float4(a[4], a[5], a[6], a[7]);
+                } else {
+                    // scalar path: group clipped by the tile, crossing a
+                    // layer boundary, or a misaligned layer
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        const int64_t f = f0 + e;
+                        if (f < lo || f >= hi) {
+                            a[e] = 0.f;
+                            continue;
+                        }
+                        while (tab.off[l + 1] <= f) ++l;
+                        const int64_t j = f - tab.off[l];
+                        float s1[1];
+                        tree_sum<WT, MAXH, 1>(
+                            W,
+                            [&](int w, float(&x)[1]) {
+                                x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
+                            },
+                            s1);
+                        float v = __fmul_rn(s1[0], u);
+                        if (resid) v = __fadd_rn(v, __ldcs(resid + f));
+                        out[f] = v;
+                        a[e] = v;
+                    }
+                }
+                tss = __fadd_rn(tss, group_sumsq(a));
+            }
+        }
+        if (partials) {
+            const double d = block_tile_sumsq(tss, red8);
+            if (threadIdx.x == 0) partials[t] = d;
+        }
+    }
+}
+
+template <class Tab, int WT, int MAXH>
+static cudaError_t launch_reduce_w(const Tab &tab, const TileGeom &G,
+                                   int64_t tiles, float u, const float *resid,
+                                   float *out, double *partials, cudaStream_t s)
+{
+    auto kern = k_reduce<Tab, WT, MAXH>;
+    const int grid = grid_for((const void *)kern, FC_BLOCK, 0, tiles);
+    kern<<<grid, FC_BLOCK, 0, s>>>(tab, G, tiles, u, resid, out, partials);
+    return cudaGetLastError();
+}
+
+template <class Tab>
+cudaError_t launch_reduce(const Tab &tab, const TileGeom &G, int64_t tiles,
+                          float u, const float *resid, float *out,
+                          double *partials, cudaStream_t s)
+{
+    switch (tab.W) {
+    case 1: return launch_reduce_w<Tab, 1, 1>(tab, G, tiles, u, resid, out, partials, s);
+    case 2: return launch_reduce_w<Tab, 2, 2>(tab, G, tiles, u, resid, out, partials, s);
+    case 4: return launch_reduce_w<Tab, 4, 3>(tab, G, tiles, u, resid, out, partials, s);
+    case 8: return launch_reduce_w<Tab, 8, 4>(tab, G, tiles, u, resid, out, partials, s);
+    case 16: return launch_reduce_w<Tab, 16, 5>(tab, G, tiles, u, resid, out, partials, s);
+    case 32: return launch_reduce_w<Tab, 32, 6>(tab, G, tiles, u, resid, out, partials, s);
+    case 64: return launch_reduce_w<Tab, 64, 7>(tab, G, tiles, u, resid, out, partials, s);
+    default: break;
+    }
+    if (tab.W < 32) return launch_reduce_w<Tab, 0, 5>(tab, G, tiles, u, resid, out, partials, s);
+    if (tab.W < 128) return launch_reduce_w<Tab, 0, 7>(tab, G, tiles, u, resid, out, partials, s);
+    return launch_reduce_w<Tab, 0, 12>(tab, G, tiles, u, resid, out, partials, s);
+}
+
+template cudaError_t launch_reduce<TableS>(const TableS &, const TileGeom &,
+                                           int64_t, float, const float *,
+                                           float *, double *, cudaStream_t);
+template cudaError_t launch_reduce<TableL>(const TableL &, const TileGeom &,
+                                           int64_t, float, const float *,
+                                           float *, double *, cudaStream_t);
+
+}  // namespace fc

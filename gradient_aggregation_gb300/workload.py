@@ -156,9 +156,18 @@ def worker_grads(wl: Workload, step: int, worker: int) -> List[np.ndarray]:
     return out
 
 
-def all_grads(wl: Workload, step: int) -> List[List[np.ndarray]]:
-    """``[worker][layer]`` fp16 arrays for one step."""
-    return [worker_grads(wl, step, w) for w in range(wl.W)]
+def all_grads(wl: Workload, step: int, threads: Optional[int] = None
+              ) -> List[List[np.ndarray]]:
+    """``[worker][layer]`` fp16 arrays for one step.  Workers are drawn on a
+    thread pool; each has its own generator, so the bits do not depend on the
+    number of threads."""
+    import concurrent.futures as cf
+    import os
+    n = threads or min(wl.W, os.cpu_count() or 1, 16)
+    if n <= 1 or wl.N * wl.W < (1 << 22):
+        return [worker_grads(wl, step, w) for w in range(wl.W)]
+    with cf.ThreadPoolExecutor(max_workers=n) as ex:
+        return list(ex.map(lambda w: worker_grads(wl, step, w), range(wl.W)))
 
 
 def initial_weights(wl: Workload) -> np.ndarray:

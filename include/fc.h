@@ -1,0 +1,245 @@
+/*
+ * fc.h — C ABI of the GB300 gradient-aggregation engine (libfc.so).
+ *
+ * One data-parallel step as FireCaffe and GradientFlow describe it, run on
+ * one GPU where W simulated workers' gradients already sit in HBM:
+ *
+ *   a1 fuse     concatenate each worker's per-layer fp16 gradients into one
+ *               buffer (GradientFlow, "Optimizing Network Performance for
+ *               Distributed DNN Training on GPU Clusters", arXiv 1902.06855,
+ *               abstract: lazy allreduce fuses many communication operations
+ *               into a single one)
+ *   a2 reduce   element-wise sum over the workers (FireCaffe, "near-linear
+ *               acceleration of deep neural network training on compute
+ *               clusters", arXiv 1511.00175, §6: allreduce of vectors of
+ *               length |dW|) in a binary reduction tree (same §6: branching
+ *               factor 2, depth log2(p)), accumulated in fp32 (mixed
+ *               precision, GradientFlow abstract) and unscaled by
+ *               1/(loss scale * W)
+ *   a3 norms    L2 norm of every fixed-size chunk of the fused vector
+ *   a4 select   keep the top-k chunks ("only transmitting important gradient
+ *               chunks", GradientFlow abstract: coarse-grained sparse
+ *               communication) and compact them
+ *   a5 update   carry unkept values in an fp32 residual; momentum SGD on the
+ *               fp32 master weights (FireCaffe §3 batched SGD, §6 each worker
+ *               applies the summed update)
+ *
+ * Readings of points the pages leave open (each implemented exactly):
+ *  - tree pairing: adjacent pairs (0,1),(2,3),... level by level; an odd last
+ *    element moves up unchanged;
+ *  - a[i] = tree_sum[i] * u + r[i] with u = binary32 nearest 1/(S*W), the
+ *    residual r added after the unscale (so it can promote a chunk);
+ *  - chunks run over the fused vector across layer boundaries; the last
+ *    chunk may be short; its score is its plain L2 norm;
+ *  - k chunks are kept; the order is larger norm first, equal norms lower
+ *    index first; k = ceil(C * num / den), at least 1;
+ *  - update (per element, kept = chunk of i is kept; every operation one
+ *    binary32 rounding, no FMA):
+ *        g = kept ? a : 0;  r = kept ? 0 : a;
+ *        v = momentum*v + lr*g;  w = w - v;  w16 = fp16_rne(w) (optional).
+ *
+ * Conventions for every call:
+ *  - Device pointers are CUDA device (or managed) memory owned by the caller;
+ *    host pointers are marked "host".  The library allocates nothing and
+ *    keeps no state between calls except the thread-local error message.
+ *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *    are asynchronous and stream-ordered; a returned FC_OK means the
+ *    arguments were valid and the kernels were launched, not that they
+ *    finished.  No call synchronises, so sequences can be captured in a
+ *    CUDA graph.  The device is the one that owns `stream` (or, for the
+ *    NULL stream, the first device pointer argument).
+ *  - fp32 arrays and fp16 outputs must be 16-byte aligned; fp16 gradient
+ *    inputs must be 2-byte aligned (16-byte aligned ones take the vector
+ *    path).  Otherwise FC_ERR_ALIGNMENT.
+ *  - Aliasing: only the pairs stated per call may alias.
+ *  - Inputs are assumed finite (no inf/NaN in the gradients).
+ *  - On error nothing is launched and fc_last_error() describes the cause.
+ *  - No kernel waits on another block or on the host, so no call can hang.
+ */
+#ifndef FC_H_
+#define FC_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define FC_API __attribute__((visibility("default")))
+#else
+#define FC_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum fc_status {
+    FC_OK = 0,
+    FC_ERR_INVALID_ARG = -1, /* null pointer, size or count out of range */
+    FC_ERR_ALIGNMENT = -2,   /* a pointer breaks the alignment rule above */
+    FC_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
+    FC_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
+    FC_ERR_LIMIT = -5        /* a table exceeds the per-launch capacity */
+} fc_status;
+
+/* Largest W*L and L that fc_fuse_pack / fc_step_reduce / fc_step accept in
+ * one call (the worker-layer pointer table travels as a kernel parameter). */
+#define FC_MAX_TABLE_PTRS 3072
+#define FC_MAX_TABLE_LAYERS 512
+
+/* Message for the last error on the calling thread ("" if none).  The string
+ * is owned by the library and valid until the next call on this thread. */
+FC_API const char *fc_last_error(void);
+
+/* Library ABI version (100 * major + minor). */
+FC_API int32_t fc_version(void);
+
+/* ---- host-only helpers (no GPU needed) ---------------------------------- */
+
+/* C = ceil(N / chunk): number of chunks of `chunk` elements over a fused
+ * vector of N elements (the last one may be short).  Returns -1 if N < 0 or
+ * chunk < 1. */
+FC_API int64_t fc_num_chunks(int64_t N, int64_t chunk);
+
+/* k = ceil(C * keep_num / keep_den) in integers, clamped to [1, C]: how many
+ * chunks the top fraction keep_num/keep_den keeps.  Returns -1 if C < 1,
+ * keep_num < 0 or keep_den < 1. */
+FC_API int64_t fc_keep_count(int64_t C, int64_t keep_num, int64_t keep_den);
+
+/* Layout of the fused buffer (a1): offsets[l] = sizes[0] + ... + sizes[l-1]
+ * (host arrays of L entries), layers in the given order with no padding;
+ * *N_out (host) = sum of the sizes.  Sizes must be >= 0 with a positive
+ * sum. */
+FC_API fc_status fc_layout(int32_t L, const int64_t *sizes, int64_t *offsets,
+                    int64_t *N_out);
+
+/* ---- a1: fuse --------------------------------------------------------------- */
+
+/* Copies W workers' L per-layer fp16 gradients into the fused buffer:
+ *   fused[w*N + offsets[l] + j] = grads[w*L + l][j],  0 <= j < sizes[l].
+ *  grads    host array of W*L device pointers to fp16, worker-major
+ *           (grads[w*L + l] is worker w's layer l); 2-byte aligned.
+ *  sizes    host [L] element counts (>= 0, sum N >= 1).
+ *  offsets  host [L] output (may be NULL): the layout as in fc_layout.
+ *  fused    device fp16 [W*N] output, 16-byte aligned; must not overlap the
+ *           gradients.
+ * W >= 1, L >= 1, W*L <= FC_MAX_TABLE_PTRS, L <= FC_MAX_TABLE_LAYERS. */
+FC_API fc_status fc_fuse_pack(const void *const *grads, int32_t W, int32_t L,
+                       const int64_t *sizes, int64_t *offsets, void *fused,
+                       void *stream);
+
+/* ---- a2: binary-tree reduction ---------------------------------------------- */
+
+/* out[i] = tree_{w=0..W-1}(fp32(fused[w*N + i])) * u  (+ residual_in[i]),
+ * u = binary32 nearest 1/(loss_scale*W), the tree as in the readings above.
+ *  fused        device fp16 [W*N] (row w = worker w), 2-byte aligned
+ *               (16-byte aligned with N % 8 == 0 takes the vector path).
+ *  residual_in  device fp32 [N] or NULL (then nothing is added).
+ *  out          device fp32 [N]; may alias residual_in (in place).
+ * W >= 1, N >= 1, loss_scale finite and > 0. */
+FC_API fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
+                         float loss_scale, const float *residual_in,
+                         float *out, void *stream);
+
+/* ---- a3: chunk norms ---------------------------------------------------------- */
+
+/* norms[c] = sqrt(sum_{i in chunk c} a[i]^2), c < C = fc_num_chunks(N, chunk).
+ * Squares and partial sums in fp32 over groups of at most 256 elements
+ * (pairs of 8, then a warp butterfly), those partials summed in fp64; the
+ * relative error is below 6e-7.  Deterministic: the same inputs give the
+ * same bits, and the same bits as the norms fc_step_select reports.
+ *  a      device fp32 [N].
+ *  norms  device fp32 [C] output. */
+FC_API fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
+                         float *norms, void *stream);
+
+/* ---- a4: top-k selection and compaction -------------------------------------- */
+
+/* Keeps the k chunks that come first in (norm descending, index ascending)
+ * order, found by a radix select on the norms' bit patterns.
+ *  norms      device fp32 [C], finite and >= 0.
+ *  a, N, chunk  the reduced gradient the norms were taken over (a device fp32
+ *             [N]); only read when packed != NULL.
+ *  idx        device int32 [k] output: kept chunk indices, ascending.
+ *  mask       device uint8 [C] output: 1 = kept.
+ *  packed     device fp32 [k*chunk] output or NULL: kept chunks' values of a
+ *             in idx order, one `chunk`-float slot each, the short last chunk
+ *             zero-padded.
+ *  threshold  device fp32 [1] output: the norm of the k-th kept chunk.
+ * 1 <= k <= C. */
+FC_API fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
+                          const float *a, int64_t N, int64_t chunk,
+                          int32_t *idx, uint8_t *mask, float *packed,
+                          float *threshold, void *stream);
+
+/* ---- a5: residual fold and momentum SGD ---------------------------------------- */
+
+/* Per element i (kept = mask[i / chunk] != 0), as in the readings above:
+ *   residual = kept ? 0 : a;  velocity = momentum*velocity + lr*(kept ? a : 0);
+ *   weights -= velocity;      weights_fp16 = fp16_rne(weights) if not NULL.
+ *  a             device fp32 [N]; may alias residual.
+ *  mask          device uint8 [C].
+ *  residual, velocity, weights  device fp32 [N], updated in place.
+ *  weights_fp16  device fp16 [N] output or NULL. */
+FC_API fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
+                                 int64_t N, int64_t chunk, float lr,
+                                 float momentum, float *residual,
+                                 float *velocity, float *weights,
+                                 void *weights_fp16, void *stream);
+
+/* ---- the fused pipeline (a1..a5 without materialising the fused buffer) ---- */
+
+/* Bytes of scratch the pipeline needs for N elements in chunks of `chunk`
+ * (per-tile partial sums of squares and the kept-slot map); 0 on bad
+ * arguments. */
+FC_API size_t fc_step_workspace_size(int64_t N, int64_t chunk);
+
+/* Phase 1 of the pipeline: a2 + the partial sums of a3, reading every
+ * worker's layer tensors in place through the layout of a1 (the fused buffer
+ * itself is never written):
+ *   a[f] = tree_w(grads[w*L + l][f - offsets[l]]) * u + residual[f]
+ * for every fused index f in layer l.  Results are bit-identical to
+ * fc_fuse_pack + fc_tree_reduce.
+ *  grads, W, L, sizes  as for fc_fuse_pack.
+ *  residual  device fp32 [N] or NULL.
+ *  a         device fp32 [N] output; may alias residual (in place).
+ *  workspace device, fc_step_workspace_size(N, chunk) bytes, 256-aligned. */
+FC_API fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
+                         const int64_t *sizes, float loss_scale,
+                         int64_t chunk, const float *residual, float *a,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Phase 2: finishes the chunk norms from the phase-1 partials (bitwise the
+ * same as fc_chunk_norms on a) and selects the top k chunks exactly as
+ * fc_chunk_select does.  norms [C], idx [k], mask [C], threshold [1] are
+ * device outputs; the kept-slot map for phase 3 goes to the workspace. */
+FC_API fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
+                         int32_t *idx, uint8_t *mask, float *threshold,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Phase 3: the a5 update of fc_residual_sgd_update, which also writes the
+ * kept chunks into `packed` (device fp32 [k*chunk] or NULL, laid out as in
+ * fc_chunk_select).  When a == residual (in place), unkept elements already
+ * hold their new residual and are neither read nor rewritten. */
+FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk, float lr,
+                         float momentum, float *residual, float *velocity,
+                         float *weights, void *weights_fp16,
+                         const uint8_t *mask, float *packed,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream);
+
+/* Phases 1-3 in one call on one stream (three kernel launches). */
+FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
+                  const int64_t *sizes, float loss_scale, int64_t chunk,
+                  int64_t k, float lr, float momentum, float *residual,
+                  float *a, float *velocity, float *weights,
+                  void *weights_fp16, float *norms, int32_t *idx,
+                  uint8_t *mask, float *packed, float *threshold,
+                  void *workspace, size_t workspace_bytes, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* FC_H_ */

@@ -102,9 +102,12 @@ void orc_fuse_pack(int32_t W, int32_t L, const int64_t *sizes,
     int64_t *off = (int64_t *)malloc(sizeof(int64_t) * (size_t)(L > 0 ? L : 1));
     int64_t N = orc_layout(L, sizes, off);
     for (int32_t w = 0; w < W; ++w)
-        for (int32_t l = 0; l < L; ++l)
-            for (int64_t j = 0; j < sizes[l]; ++j)
-                fused[(int64_t)w * N + off[l] + j] = grads[(int64_t)w * L + l][j];
+        for (int32_t l = 0; l < L; ++l) {
+            const uint16_t *src = grads[(int64_t)w * L + l];
+            uint16_t *dst = fused + (int64_t)w * N + off[l];
+            const int64_t n = sizes[l];
+            for (int64_t j = 0; j < n; ++j) dst[j] = src[j];
+        }
     free(off);
 }
 
@@ -143,11 +146,19 @@ float orc_unscale_factor(float loss_scale, int32_t W)
 void orc_tree_reduce(int32_t W, int64_t N, const uint16_t *fused,
                      float loss_scale, const float *residual, float *out)
 {
+    /* orc_half_to_float of every bit pattern, looked up instead of
+     * recomputed per element (the values are identical). */
+    static float h2f[65536];
+    static int h2f_ready = 0;
+    if (!h2f_ready) {
+        for (int b = 0; b < 65536; ++b) h2f[b] = orc_half_to_float((uint16_t)b);
+        h2f_ready = 1;
+    }
     float *x = (float *)malloc(sizeof(float) * (size_t)W);
     float inv = orc_unscale_factor(loss_scale, W);
     for (int64_t i = 0; i < N; ++i) {
         for (int32_t w = 0; w < W; ++w)
-            x[w] = orc_half_to_float(fused[(int64_t)w * N + i]);
+            x[w] = h2f[fused[(int64_t)w * N + i]];
         float s = orc_tree_sum(x, W);
         float a = s * inv;
         if (residual) a = a + residual[i];

@@ -31,5 +31,5 @@ def fc_lib():
     """The CUDA library, built in-tree if it is missing."""
     from gradient_aggregation_gb300 import build as fcbuild
     fcbuild.build_library()
-    from gradient_aggregation_gb300 import _fc
-    return _fc.lib()
+    from gradient_aggregation_gb300 import fc
+    return fc.lib()

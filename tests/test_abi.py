@@ -1,0 +1,126 @@
+"""The C ABI without a GPU: the library builds and loads, exports every entry
+point that include/fc.h declares, computes the host-side layout and counts,
+and rejects bad arguments with a status before touching any device."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from tests.conftest import ROOT, read_golden
+
+HEADER = os.path.join(ROOT, "include", "fc.h")
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"FC_API\s+[\w\s\*]+?\b(fc_\w+)\s*\(", text)))
+
+
+def test_header_declares_the_five_calls_and_the_pipeline():
+    names = declared_functions()
+    for n in ["fc_fuse_pack", "fc_tree_reduce", "fc_chunk_norms", "fc_chunk_select",
+              "fc_residual_sgd_update", "fc_step", "fc_step_reduce", "fc_step_select",
+              "fc_step_update", "fc_step_workspace_size", "fc_last_error"]:
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(fc_lib):
+    for name in declared_functions():
+        assert hasattr(fc_lib, name), name
+
+
+def test_num_chunks_and_keep_counts(fc_lib):
+    from gradient_aggregation_gb300 import fc
+    for name, N, cs, C, p, k, last in read_golden("workload_counts.txt"):
+        assert fc.fc_num_chunks(int(N), int(cs)) == int(C)
+        assert fc.fc_keep_count(int(C), int(p), 100) == int(k)
+    assert fc.fc_num_chunks(0, 4) == 0
+    assert fc.fc_num_chunks(5, 0) == -1
+    assert fc.fc_keep_count(10, 0, 100) == 1
+    assert fc.fc_keep_count(10, 250, 100) == 10
+    assert fc.fc_keep_count(0, 1, 1) == -1
+
+
+def test_layout_matches_hand_worked_offsets(fc_lib):
+    from gradient_aggregation_gb300 import fc
+    rows = read_golden("alexnet_offsets.txt")
+    sizes = [int(r[1]) for r in rows[:-1]]
+    off, n = fc.fc_layout(sizes)
+    assert off == [int(r[2]) for r in rows[:-1]]
+    assert n == int(rows[-1][1])
+    assert fc.fc_layout([0, 3, 0, 2]) == ([0, 0, 3, 3], 5)
+
+
+def _status(fn, *args):
+    return int(fn(*args))
+
+
+def test_argument_errors_return_before_any_device_work(fc_lib):
+    from gradient_aggregation_gb300 import fc
+    L = fc_lib
+    P = ctypes.c_void_p
+    fake = 0x10000          # never dereferenced: every case fails validation
+    odd = 0x10002           # 2-byte aligned only
+
+    def grads(n, p=fake):
+        arr = (ctypes.c_void_p * n)(*([p] * n))
+        return ctypes.cast(arr, P), arr
+
+    sizes = (ctypes.c_int64 * 2)(8, 8)
+    g, keep = grads(4)
+    # fuse pack
+    assert L.fc_fuse_pack(None, 2, 2, ctypes.cast(sizes, P), None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_fuse_pack(g, 0, 2, ctypes.cast(sizes, P), None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_fuse_pack(g, 2, 2, ctypes.cast(sizes, P), None, None, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_fuse_pack(g, 2, 2, ctypes.cast(sizes, P), None, odd, None) == fc.FC_ERR_ALIGNMENT
+    gm, keep2 = grads(4, 0x10001)
+    assert L.fc_fuse_pack(gm, 2, 2, ctypes.cast(sizes, P), None, fake, None) == fc.FC_ERR_ALIGNMENT
+    big = 1600
+    gb, keep3 = grads(big * 2)
+    sizes2 = (ctypes.c_int64 * 2)(8, 8)
+    assert L.fc_fuse_pack(gb, big, 2, ctypes.cast(sizes2, P), None, fake, None) == fc.FC_ERR_LIMIT
+    assert b"FC_MAX_TABLE_PTRS" in L.fc_last_error()
+    neg = (ctypes.c_int64 * 2)(8, -1)
+    assert L.fc_fuse_pack(g, 2, 2, ctypes.cast(neg, P), None, fake, None) == fc.FC_ERR_INVALID_ARG
+    # tree reduce
+    assert L.fc_tree_reduce(fake, 0, 10, 1.0, None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_tree_reduce(fake, 2, 0, 1.0, None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_tree_reduce(fake, 2, 10, 0.0, None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_tree_reduce(fake, 2, 10, float("inf"), None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_tree_reduce(fake, 2, 10, 1.0, None, fake + 4, None) == fc.FC_ERR_ALIGNMENT
+    assert L.fc_tree_reduce(fake + 1, 2, 10, 1.0, None, fake, None) == fc.FC_ERR_ALIGNMENT
+    # norms
+    assert L.fc_chunk_norms(fake, 10, 0, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_norms(fake + 8, 10, 4, fake, None) == fc.FC_ERR_ALIGNMENT
+    # select
+    assert L.fc_chunk_select(fake, 4, 5, None, 0, 0, fake, fake, None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 0, None, 0, 0, fake, fake, None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 2, None, 0, 0, None, fake, None, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 2, fake, 100, 10, fake, fake, fake, fake, None) == fc.FC_ERR_INVALID_ARG
+    # update
+    assert L.fc_residual_sgd_update(fake, fake, 10, 0, 0.1, 0.9, fake, fake, fake, None, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_residual_sgd_update(fake, None, 10, 2, 0.1, 0.9, fake, fake, fake, None, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_residual_sgd_update(fake, fake, 10, 2, float("nan"), 0.9, fake, fake, fake, None, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_residual_sgd_update(fake, fake, 10, 2, 0.1, 0.9, fake, fake + 4, fake, None, None) == fc.FC_ERR_ALIGNMENT
+    # pipeline workspace
+    ws = fc.fc_step_workspace_size(1000, 64)
+    assert ws > 0 and ws % 256 == 0
+    assert fc.fc_step_workspace_size(0, 64) == 0
+    assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, fake, None, 0, None) == fc.FC_ERR_WORKSPACE
+    assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, fake, fake, 1, None) == fc.FC_ERR_WORKSPACE
+    assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, fake, fake + 16, 10 ** 6, None) == fc.FC_ERR_ALIGNMENT
+    assert L.fc_step_select(16, 4, 9, fake, fake, fake, fake, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_step_update(fake, 16, 4, 0.1, 0.9, fake, fake, fake, None, fake, fake + 4, fake, 10 ** 6, None) == fc.FC_ERR_ALIGNMENT
+    assert L.fc_step(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, 5, 0.1, 0.9, fake, fake, fake, fake,
+                     None, fake, fake, fake, None, fake, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
+    assert b"k = 5" in L.fc_last_error()
+
+
+def test_python_binding_raises_with_message(fc_lib):
+    from gradient_aggregation_gb300 import fc
+    with pytest.raises(fc.FcError) as e:
+        fc._check(fc_lib.fc_tree_reduce(0x10000, 0, 10, 1.0, None, 0x10000, None))
+    assert e.value.status == fc.FC_ERR_INVALID_ARG and "W = 0" in str(e.value)

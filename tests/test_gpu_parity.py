@@ -1,0 +1,237 @@
+"""GPU parity: the CUDA library (through its C ABI) against the CPU oracle.
+
+Covers the five workloads at full size with state carried over their steps,
+both the fused pipeline (fc_step) and the five separate calls, and small
+random shapes that span several tiles with ragged tails, odd worker counts,
+layers that break 16-byte alignment, short last chunks, ties, a single
+element and the degenerate keep-all / keep-one cases.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gradient_aggregation_gb300 import fc, workload
+from tests.gpu_util import GpuRun, bits_equal, dev_grads, oracle_step
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(fc_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+
+
+def _compare_paths(p, s):
+    for key in ("a", "norms", "idx", "mask", "threshold", "residual", "velocity",
+                "weights", "packed", "w16"):
+        if key in p and key in s:
+            assert bits_equal(np.asarray(p[key]), np.asarray(s[key])), key
+
+
+def _run_workload(wl, steps=None, both_paths=True):
+    steps = wl.steps if steps is None else steps
+    runs = [GpuRun(wl, "pipeline")]
+    if both_paths:
+        runs.append(GpuRun(wl, "separate"))
+    st = oracle.State(workload.initial_weights(wl))
+    reports = []
+    for s in range(steps):
+        g_np = workload.all_grads(wl, s)
+        g_dev = dev_grads(g_np)
+        snaps = []
+        for r in runs:
+            r.step(g_dev)
+            snaps.append(r.snapshot())
+        del g_dev
+        if both_paths:
+            _compare_paths(snaps[0], snaps[1])
+            assert runs[1].offsets == list(oracle.layout(wl.sizes)[0])
+        reports.append(oracle_step(g_np, st, wl, snaps[-1]))
+        del g_np, snaps
+    torch.cuda.empty_cache()
+    return reports
+
+
+@pytest.mark.parametrize("name", ["tiny", "nin", "googlenet", "alexnet", "stress"])
+def test_workload_parity(name):
+    wl = workload.get(name)
+    reports = _run_workload(wl, both_paths=name != "stress")
+    assert len(reports) == wl.steps
+
+
+SMALL_CASES = [
+    # W, sizes, chunk, keep percent
+    (1, [1], 1, 100),
+    (1, [7], 3, 50),
+    (2, [9, 4], 4, 50),
+    (3, [1000], 8, 10),
+    (5, [17, 33, 1, 2048, 5], 100, 30),
+    (7, [4096, 3, 4099], 2048, 40),
+    (8, [2049, 2047], 2049, 50),
+    (9, [12345], 5000, 67),
+    (16, [96, 130, 1, 8, 7, 4000], 256, 25),
+    (17, [3000, 3001], 64, 10),
+    (33, [513, 1027], 512, 20),
+    (64, [20000], 4096, 10),
+    (65, [999], 128, 90),
+    (4, [3, 0, 5, 0, 8], 2, 60),
+    (2, [100000], 32768, 1),
+]
+
+
+@pytest.mark.parametrize("case", SMALL_CASES, ids=[str(i) for i in range(len(SMALL_CASES))])
+def test_small_shapes(case):
+    W, sizes, chunk, keep = case
+    wl = workload.custom(W=W, sizes=sizes, chunk=chunk, keep_percent=keep,
+                         config_id=100 + W, steps=3, loss_scale=1000.0)
+    _run_workload(wl)
+
+
+def test_heavy_tail_small():
+    wl = workload.custom(W=8, sizes=[50000, 3], chunk=512, keep_percent=10,
+                         heavy_tail=True, grad_std=1e-3, steps=3, config_id=140)
+    _run_workload(wl)
+
+
+def test_misaligned_gradient_pointers():
+    """Layer tensors that start 2 bytes past a 16-byte boundary take the
+    element-wise path and still match."""
+    wl = workload.custom(W=6, sizes=[1001, 64, 3333], chunk=300, keep_percent=20,
+                         config_id=150, steps=2)
+    st = oracle.State(workload.initial_weights(wl))
+    run = GpuRun(wl, "pipeline")
+    sep = GpuRun(wl, "separate")
+    for s in range(2):
+        g_np = workload.all_grads(wl, s)
+        g_dev = []
+        for row in g_np:
+            r = []
+            for g in row:
+                buf = torch.empty(g.size + 1, dtype=torch.float16, device="cuda")
+                view = buf[1:]
+                view.copy_(torch.from_numpy(g))
+                assert view.data_ptr() % 16 == 2
+                r.append(view)
+            g_dev.append(r)
+        run.step(g_dev)
+        sep.step(g_dev)
+        a, b = run.snapshot(), sep.snapshot()
+        _compare_paths(a, b)
+        oracle_step(g_np, st, wl, b)
+
+
+def test_fused_buffer_with_ragged_rows():
+    """N % 8 != 0: the fused rows are not 16-byte aligned."""
+    wl = workload.custom(W=3, sizes=[1234, 7], chunk=100, keep_percent=50,
+                         config_id=151, steps=1)
+    g_np = workload.all_grads(wl, 0)
+    run = GpuRun(wl, "separate")
+    run.step(dev_grads(g_np))
+    oracle_step(g_np, oracle.State(workload.initial_weights(wl)), wl, run.snapshot())
+
+
+def test_ties_keep_lowest_indices():
+    """Every chunk has the same norm: the k lowest chunk indices are kept."""
+    W, N, cs = 4, 64 * 10, 64
+    wl = workload.custom(W=W, sizes=[N], chunk=cs, keep_percent=30, config_id=152)
+    g = [[np.full(N, 2.0, dtype=np.float16)] for _ in range(W)]
+    for path in ("pipeline", "separate"):
+        run = GpuRun(wl, path)
+        run.step(dev_grads(g))
+        snap = run.snapshot()
+        assert list(snap["idx"]) == [0, 1, 2]
+        oracle_step(g, oracle.State(workload.initial_weights(wl)), wl, snap)
+
+
+def test_keep_one_and_partial_last_chunk_padding():
+    wl = workload.custom(W=2, sizes=[1000], chunk=300, keep_percent=1, config_id=153)
+    g = [[np.zeros(1000, np.float16)] for _ in range(2)]
+    g[0][0][950:] = 4.0       # the short last chunk (100 elements) wins
+    run = GpuRun(wl, "pipeline")
+    run.packed.fill_(7.0)
+    run.step(dev_grads(g))
+    snap = run.snapshot()
+    assert list(snap["idx"]) == [3]
+    assert np.all(snap["packed"][100:] == 0.0)
+    oracle_step(g, oracle.State(workload.initial_weights(wl)), wl, snap)
+
+
+def test_inplace_matches_out_of_place_and_is_deterministic():
+    wl = workload.custom(W=16, sizes=[40000, 123, 70001], chunk=4096, keep_percent=25,
+                         config_id=154, steps=3)
+    runs = [GpuRun(wl, "pipeline", inplace=True), GpuRun(wl, "pipeline", inplace=False),
+            GpuRun(wl, "pipeline", inplace=True)]
+    for s in range(3):
+        g = dev_grads(workload.all_grads(wl, s))
+        snaps = []
+        for r in runs:
+            r.step(g)
+            snaps.append(r.snapshot())
+        for other in snaps[1:]:
+            for key in ("residual", "velocity", "weights", "idx", "mask", "norms",
+                        "packed", "w16", "threshold"):
+                assert bits_equal(np.asarray(snaps[0][key]), np.asarray(other[key])), key
+
+
+def test_checkpoint_resume_is_bit_exact():
+    wl = workload.custom(W=8, sizes=[30000, 5000], chunk=1024, keep_percent=20,
+                         config_id=155, steps=5)
+    grads = [dev_grads(workload.all_grads(wl, s)) for s in range(5)]
+    straight = GpuRun(wl, "pipeline", inplace=True)
+    for s in range(5):
+        straight.step(grads[s])
+    end = straight.snapshot()
+    first = GpuRun(wl, "pipeline", inplace=True)
+    for s in range(3):
+        first.step(grads[s])
+    torch.cuda.synchronize()
+    saved = {k: getattr(first, k).cpu().clone() for k in ("residual", "velocity", "weights")}
+    resumed = GpuRun(wl, "pipeline", inplace=True)
+    for k, v in saved.items():
+        getattr(resumed, k).copy_(v.cuda())
+    for s in range(3, 5):
+        resumed.step(grads[s])
+    got = resumed.snapshot()
+    for key in ("residual", "velocity", "weights", "idx", "w16"):
+        assert bits_equal(end[key], got[key]), key
+
+
+def test_cuda_graph_replay_matches_eager():
+    wl = workload.custom(W=4, sizes=[5000, 77], chunk=256, keep_percent=10,
+                         config_id=156, steps=3)
+    grads = dev_grads(workload.all_grads(wl, 0))
+    eager = GpuRun(wl, "pipeline", inplace=True)
+    graphed = GpuRun(wl, "pipeline", inplace=True)
+    table = fc.PtrTable(grads)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        graphed.step(table, s)          # warm-up outside capture (step 1)
+    torch.cuda.current_stream().wait_stream(s)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        graphed.step(table)
+    eager.step(grads)
+    for _ in range(3):                  # steps 2..4
+        eager.step(grads)
+        g.replay()
+    a, b = eager.snapshot(), graphed.snapshot()
+    for key in ("residual", "velocity", "weights", "idx", "norms"):
+        assert bits_equal(a[key], b[key]), key
+
+
+def test_device_argument_errors():
+    dev = "cuda"
+    a = torch.zeros(1000, dtype=torch.float32, device=dev)
+    with pytest.raises(fc.FcError) as e:
+        fc.fc_chunk_norms(a[1:], 999, 10, torch.empty(100, device=dev))
+    assert e.value.status == fc.FC_ERR_ALIGNMENT
+    wl = workload.custom(W=2, sizes=[1000], chunk=100, keep_percent=10, config_id=157)
+    run = GpuRun(wl, "pipeline")
+    run.ws = run.ws[:16]
+    with pytest.raises(fc.FcError) as e:
+        run.step(dev_grads(workload.all_grads(wl, 0)))
+    assert e.value.status == fc.FC_ERR_WORKSPACE
