@@ -1,0 +1,459 @@
+"""Benchmark of the gradient-aggregation engine on GB300.
+
+One step = the whole hot path over one batch of synthetic gradients: the
+workers' per-layer fp16 gradients are fused (through the layout, without a
+copy), tree-reduced in fp32 with the loss-scale/W unscale and the residual,
+scored by chunk L2 norm, the top chunks selected and compacted, and the
+residual/momentum-SGD update applied (three kernels: fc_step).
+
+Metric: worker-gradient GB/s = W * N * 2 bytes per step / time per step.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--workload alexnet]
+                  [--impl reference]
+
+With torchrun (N > 1) every rank runs an independent replica of the same
+workload on its own GPU (the method has no cross-GPU exchange here): the
+value is all ranks' bytes over the slowest rank's time.
+
+`--impl reference` times the CPU oracle (single-threaded C, the plain
+statement of the method) on a bounded sample of the same workload per step.
+"""
+
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+from gradient_aggregation_gb300 import workload  # noqa: E402
+
+METRIC = "worker-gradient GB/s aggregated (1xGB300) and % of HBM roofline vs CPU oracle"
+UNIT = "GB/s"
+TILE = 2048  # elements per tile of the kernels (FC_TILE)
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=2000)
+    p.add_argument("--warmup", type=int, default=20)
+    p.add_argument("--workload", default="alexnet", choices=sorted(workload.WORKLOADS))
+    p.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    p.add_argument("--elements", type=int, default=0,
+                   help="use only the first ELEMENTS fused elements of the workload "
+                        "(small cases for profiling)")
+    p.add_argument("--e2e-steps", type=int, default=20)
+    p.add_argument("--no-cpu-baseline", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=8.0,
+                   help="target CPU time of the oracle baseline sample")
+    return p.parse_args()
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def config_of(wl, extra=None):
+    C = -(-wl.N // wl.chunk)
+    cfg = {"workload": "%s-shaped: W=%d workers, N=%d fp16 elements in %d layer tensors, "
+                       "chunk %d, keep %d%%" % (wl.name, wl.W, wl.N, wl.L, wl.chunk,
+                                                wl.keep_percent),
+           "W": wl.W, "N": wl.N, "layers": wl.L, "chunk": wl.chunk, "chunks": C,
+           "keep_percent": wl.keep_percent, "loss_scale": wl.loss_scale,
+           "lr": wl.lr, "momentum": wl.momentum}
+    if extra:
+        cfg.update(extra)
+    return cfg
+
+
+# ---- CPU oracle samples ---------------------------------------------------------
+
+def sample_workload(wl, m):
+    """The first m fused elements of wl: layers cut at m."""
+    sizes, acc = [], 0
+    for s in wl.sizes:
+        if acc >= m:
+            break
+        take = min(s, m - acc)
+        sizes.append(take)
+        acc += take
+    return workload.custom(W=wl.W, sizes=sizes, chunk=wl.chunk,
+                           keep_percent=wl.keep_percent, loss_scale=wl.loss_scale,
+                           grad_std=wl.grad_std, momentum=wl.momentum, lr=wl.lr,
+                           config_id=wl.config_id, heavy_tail=wl.heavy_tail)
+
+
+def oracle_step_time(wl_s, grads, state):
+    import oracle
+    t0 = time.perf_counter()
+    oracle.step(grads, state, wl_s.loss_scale, wl_s.chunk, wl_s.keep_percent, 100,
+                wl_s.lr, wl_s.momentum)
+    return time.perf_counter() - t0
+
+
+def oracle_elems_for(wl, seconds):
+    """Calibrate how many fused elements the oracle handles in `seconds`."""
+    import oracle
+    m = min(wl.N, 1 << 18)
+    ws = sample_workload(wl, m)
+    g = workload.all_grads(ws, 0)
+    st = oracle.State(workload.initial_weights(ws))
+    oracle_step_time(ws, g, st)                    # warm (page faults, table)
+    t = min(oracle_step_time(ws, g, st) for _ in range(2))
+    return max(1024, min(wl.N, int(m * seconds / max(t, 1e-6))))
+
+
+def cpu_baseline(wl, seconds):
+    import oracle
+    m = oracle_elems_for(wl, seconds)
+    ws = sample_workload(wl, m)
+    g = workload.all_grads(ws, 0)
+    st = oracle.State(workload.initial_weights(ws))
+    t = oracle_step_time(ws, g, st)
+    gbs = ws.W * ws.N * 2 / t / 1e9
+    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+            "sample": "one step of the oracle (pack, tree reduce, norms, select, update) on "
+                      "the first %d of %d fused elements of every worker (%.1f%%), %.2f s"
+                      % (ws.N, wl.N, 100.0 * ws.N / wl.N, t)}
+
+
+def run_reference(args, wl, rank):
+    if rank != 0:
+        return 0
+    import oracle
+    budget = 90.0 / max(1, args.steps + args.warmup)
+    m = oracle_elems_for(wl, budget)
+    ws = sample_workload(wl, m)
+    g = workload.all_grads(ws, 0)
+    st = oracle.State(workload.initial_weights(ws))
+    for _ in range(args.warmup):
+        oracle_step_time(ws, g, st)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle_step_time(ws, g, st)
+    dt = time.perf_counter() - t0
+    value = ws.W * ws.N * 2 * args.steps / dt / 1e9
+    sample = ("each step: the oracle (single-threaded C) on the first %d of %d fused "
+              "elements of every worker" % (ws.N, wl.N))
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": UNIT,
+            "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(dt / args.steps * 1e3, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+            "data": "synthetic (seeded Gaussian fp16 gradients, workload-shaped)",
+            "config": config_of(wl, {"sample_elements": ws.N}),
+            "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---- clocks -------------------------------------------------------------------------
+
+class ClockSampler:
+    FIELDS = ("timestamp,uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid, out_path=None):
+        self.uuid = uuid
+        self.rows = []
+        self.out_path = out_path
+        self.proc = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.rows.append((time.time(), [x.strip() for x in line.split(",")]))
+
+    def stop(self):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        mine = [r for (t, r) in self.rows if len(r) >= 10 and (not self.uuid or r[1] == self.uuid)]
+        during = [r for (t, r) in self.rows
+                  if t0 <= t <= t1 + 0.15 and len(r) >= 10 and (not self.uuid or r[1] == self.uuid)]
+        use = during if during else mine[-3:]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[2]) for r in use if r[2].replace(".", "").isdigit()]
+        mx = [float(r[3]) for r in use if r[3].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[6 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(use), "in_timed_region": bool(during)}
+
+
+# ---- GPU arm ---------------------------------------------------------------------------
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for name in ("fc_reduce.cu", "fc_common.cuh"):
+        with open(os.path.join(ROOT, "gradient_aggregation_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_from_profile(src_hash, wl):
+    """DRAM bytes per launch of the reduction kernel from the committed ncu
+    summary, if it was taken on the current kernel source."""
+    path = os.path.join(ROOT, "profiles", "k_reduce_%s.md" % wl.name)
+    if not os.path.exists(path):
+        return None
+    vals = {}
+    with open(path) as f:
+        for line in f:
+            if ":" in line and line.startswith("- "):
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("kernel_source_sha") != src_hash:
+        return None
+    try:
+        return float(vals["dram_bytes_per_full_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def run_gpu(args, wl, rank, world, local):
+    import torch
+    from gradient_aggregation_gb300 import fc
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def max_over_ranks(x):
+        if world == 1:
+            return x
+        import torch.distributed as dist
+        t = torch.tensor([x], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+
+    fc.lib()
+    W, N = wl.W, wl.N
+    grads_np = workload.all_grads(wl, 0)
+    # per-layer device tensors, as a training framework's autograd leaves them
+    grads = [[torch.from_numpy(g).to(dev) for g in row] for row in grads_np]
+    table = fc.PtrTable(grads)
+    eng = fc.Engine(wl.sizes, W, wl.chunk, wl.keep_percent, 100, wl.loss_scale, wl.lr,
+                    wl.momentum, torch.from_numpy(workload.initial_weights(wl)).to(dev))
+    s = torch.cuda.Stream(device=dev)
+    phases = list(eng.phases(table, s))
+
+    def step_phased(evs=None):
+        if evs is not None:
+            evs[0].record(s)
+        phases[0]()
+        if evs is not None:
+            evs[1].record(s)
+        phases[1]()
+        phases[2]()
+
+    torch.cuda.synchronize()
+    for _ in range(max(3, args.warmup)):
+        step_phased()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+           for _ in range(K)]
+    start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+        if not uuid.startswith("GPU-"):
+            uuid = "GPU-" + uuid
+    except Exception:
+        uuid = None
+    sampler = ClockSampler(uuid)
+    sampler.start()
+    time.sleep(0.35)
+    barrier()
+    torch.cuda.synchronize()
+    t_wall0 = time.time()
+    start.record(s)
+    for i in range(K):
+        step_phased(evs[i])
+    end.record(s)
+    torch.cuda.synchronize()
+    t_wall1 = time.time()
+    barrier()
+    time.sleep(0.25)
+    sampler.stop()
+    clocks = sampler.summary(t_wall0, t_wall1)
+
+    total_ms = start.elapsed_time(end)
+    reduce_ms = [a.elapsed_time(b) for (a, b) in evs]
+    t_max = max_over_ranks(total_ms / 1e3)
+    step_bytes = W * N * 2
+    value = world * step_bytes * K / t_max / 1e9
+    ms_per_step = t_max * 1e3 / K
+
+    # roofline of the dominant kernel (phase 1: tree reduce + norm partials)
+    C = -(-N // wl.chunk)
+    P = -(-wl.chunk // TILE)
+    k_alg = W * N * 2 + 4 * N + 4 * N + 8 * C * P
+    k_ms = statistics.mean(reduce_ms)
+    peaks = {}
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peaks = json.load(f)
+    except OSError:
+        pass
+    peak = float(peaks.get("hbm_gbs", 6800.0))
+    peak_src = "measured" if "hbm_gbs" in peaks else "fallback"
+    achieved = k_alg / (k_ms / 1e3) / 1e9
+    src_hash = kernel_source_hash()
+    traffic = traffic_from_profile(src_hash, wl)
+
+    # the rest of the step: select + update, measured as step minus phase 1
+    rest_ms = ms_per_step - k_ms
+    kept_frac = eng.k * wl.chunk / N
+    update_alg = N * (16 + 8 * min(1.0, kept_frac))    # in place: v,w r/w; kept: a, r, packed
+    step_alg = k_alg + update_alg
+
+    # end to end: pinned host gradients -> device, step, result back to host
+    e2e = None
+    if args.e2e_steps > 0:
+        host = torch.empty(W * N, dtype=torch.float16, pin_memory=True)
+        hv = host.numpy()
+        pos = 0
+        for row in grads_np:
+            for g in row:
+                hv[pos:pos + g.size] = g
+                pos += g.size
+        stage = torch.empty(W * N, dtype=torch.float16, device=dev)
+        views, pos = [], 0
+        for w in range(W):
+            r = []
+            for n in wl.sizes:
+                r.append(stage[pos:pos + n])
+                pos += n
+            views.append(r)
+        etable = fc.PtrTable(views)
+        res_idx = torch.empty(eng.k, dtype=torch.int32, pin_memory=True)
+        res_thr = torch.empty(1, dtype=torch.float32, pin_memory=True)
+        for _ in range(2):
+            with torch.cuda.stream(s):
+                stage.copy_(host, non_blocking=True)
+            eng.step(etable, s)
+            with torch.cuda.stream(s):
+                res_idx.copy_(eng.idx, non_blocking=True)
+                res_thr.copy_(eng.threshold, non_blocking=True)
+            s.synchronize()
+        barrier()
+        E = args.e2e_steps
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        e0.record(s)
+        for _ in range(E):
+            with torch.cuda.stream(s):
+                stage.copy_(host, non_blocking=True)
+            eng.step(etable, s)
+            with torch.cuda.stream(s):
+                res_idx.copy_(eng.idx, non_blocking=True)
+                res_thr.copy_(eng.threshold, non_blocking=True)
+            s.synchronize()         # the host reads the step's result
+            _ = int(res_idx[0]), float(res_thr[0])
+        e1.record(s)
+        torch.cuda.synchronize()
+        et = max_over_ranks(e0.elapsed_time(e1) / 1e3)
+        e2e = {"value": round(world * step_bytes * E / et / 1e9, 3), "unit": UNIT,
+               "h2d_bytes_per_step": W * N * 2, "d2h_bytes_per_step": 4 * eng.k + 4,
+               "steps": E, "ms_per_step": round(et * 1e3 / E, 4),
+               "path": "one pinned-host -> device copy of all workers' gradients, fc_step, "
+                       "kept indices + threshold copied back and read on the host"}
+        del host, stage
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = cpu_baseline(wl, args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
+            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f32", "data": "synthetic (seeded Gaussian fp16 gradients, workload-shaped)",
+            "config": config_of(wl, {
+                "parallelism": "replicas" if world > 1 else "single GPU",
+                "path": "fc_step: pack-elided tree reduce + norm partials, radix top-k select, "
+                        "residual/momentum-SGD update with packed kept chunks (3 kernels)",
+                "l2": "inputs larger than L2: %.2f GB fp16 gradients + %.2f GB fp32 state per step"
+                      % (step_bytes / 1e9, 12 * N / 1e9)}),
+            "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                         "unit": "GB/s", "frac": round(achieved / peak, 4),
+                         "traffic": traffic, "kernel": "k_reduce (fc_step_reduce)",
+                         "algorithmic_bytes_per_launch": k_alg,
+                         "avg_launch_ms": round(k_ms, 5), "peak_source": peak_src + " hbm_gbs"},
+            "step_roofline": {"algorithmic_bytes_per_step": int(step_alg),
+                              "achieved_gbs": round(step_alg / (ms_per_step / 1e3) / 1e9, 1),
+                              "frac": round(step_alg / (ms_per_step / 1e3) / 1e9 / peak, 4),
+                              "select_update_ms": round(rest_ms, 5)},
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": 3 * K,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_env()
+    wl = workload.get(args.workload)
+    if args.elements:
+        wl = sample_workload(wl, args.elements)
+    if args.impl == "reference":
+        return run_reference(args, wl, rank)
+    return run_gpu(args, wl, rank, world, local)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

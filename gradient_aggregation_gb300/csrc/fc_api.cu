@@ -38,28 +38,23 @@ fc_status cuda_fail(cudaError_t e, const char *what)
 
 bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-// Makes the device that owns `stream` (or `ptr` for the NULL stream) current.
+// Makes the device that owns `ptr` (a device pointer argument of the call)
+// current.  Only queries that are legal while a stream is being captured
+// into a CUDA graph are used.
 fc_status bind_device(void *stream, const void *ptr)
 {
+    (void)stream;
     (void)cudaGetLastError();  // clear a stale error of this runtime
-    int dev = -1;
-    cudaError_t e;
-    if (stream) {
-        e = cudaStreamGetDevice((cudaStream_t)stream, &dev);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaStreamGetDevice");
-    } else {
-        cudaPointerAttributes at;
-        e = cudaPointerGetAttributes(&at, ptr);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
-        if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
-            return fail(FC_ERR_INVALID_ARG, "pointer %p is not device memory", ptr);
-        dev = at.device;
-    }
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return fail(FC_ERR_INVALID_ARG, "pointer %p is not device memory", ptr);
     int cur = -1;
     e = cudaGetDevice(&cur);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (cur != dev) {
-        e = cudaSetDevice(dev);
+    if (cur != at.device) {
+        e = cudaSetDevice(at.device);
         if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
     }
     return FC_OK;
@@ -76,9 +71,37 @@ TileGeom geom(int64_t N, int64_t cs)
     return G;
 }
 
+UnitGeom ugeom(int64_t N, int64_t cs)
+{
+    UnitGeom G;
+    G.N = N;
+    G.cs = cs;
+    G.C = ceil_div(N, cs);
+    G.U = ceil_div(cs, FC_UNIT);
+    const int64_t last = N - (G.C - 1) * cs;
+    G.units = (G.C - 1) * G.U + ceil_div(last, FC_UNIT);
+    return G;
+}
+
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-size_t ws_partials_bytes(int64_t C, int64_t P) { return align256((size_t)(C * P) * sizeof(double)); }
+// Workspace of the pipeline: unit sums (float [units]), the selection's
+// count of finished blocks (zero between calls) and the kept-slot map
+// (int32 [C]).
+struct WsLayout {
+    size_t partials, counters, slot, total;
+};
+
+WsLayout ws_layout(int64_t N, int64_t cs)
+{
+    const UnitGeom G = ugeom(N, cs);
+    WsLayout l;
+    l.partials = 0;
+    l.counters = align256((size_t)G.units * sizeof(float));
+    l.slot = l.counters + 256;
+    l.total = l.slot + align256((size_t)G.C * sizeof(int32_t));
+    return l;
+}
 
 fc_status check_sizes(int32_t L, const int64_t *sizes, int64_t *N_out)
 {
@@ -118,13 +141,6 @@ fc_status check_table(const void *const *grads, int32_t W, int32_t L,
 bool fits_small(int32_t W, int32_t L)
 {
     return L <= 64 && (int64_t)W * L <= 256;
-}
-
-const void *first_nonnull(const void *const *grads, int64_t n)
-{
-    for (int64_t i = 0; i < n; ++i)
-        if (grads[i]) return grads[i];
-    return nullptr;
 }
 
 fc_status check_f32(const void *p, const char *name, bool may_be_null)
@@ -220,8 +236,7 @@ fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
     TRY(check_f32(out, "out", false));
     TRY(bind_device(stream, out));
     const float u = (float)(1.0 / ((double)loss_scale * (double)W));
-    const TileGeom G = geom(N, FC_TILE);
-    const int64_t tiles = ceil_div(N, FC_TILE);
+    const UnitGeom G = ugeom(N, N);  // one chunk: no norms here
     const int64_t sizes[1] = {N};
     cudaError_t e;
     // one "layer" per worker: row w of the fused buffer
@@ -230,13 +245,13 @@ fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
         const void *rows[256];
         for (int w = 0; w < W; ++w) rows[w] = (const __half *)fused + (int64_t)w * N;
         fill_table(tab, rows, W, 1, sizes);
-        e = launch_reduce(tab, G, tiles, u, residual_in, out, nullptr, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual_in, out, nullptr, (cudaStream_t)stream);
     } else {
         static thread_local TableL tab;
         static thread_local const void *rows[FC_MAX_TABLE_PTRS];
         for (int w = 0; w < W; ++w) rows[w] = (const __half *)fused + (int64_t)w * N;
         fill_table(tab, rows, W, 1, sizes);
-        e = launch_reduce(tab, G, tiles, u, residual_in, out, nullptr, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual_in, out, nullptr, (cudaStream_t)stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "tree_reduce launch");
     return ok();
@@ -250,8 +265,7 @@ fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
     TRY(check_f32(a, "a", false));
     TRY(check_f32(norms, "norms", false));
     TRY(bind_device(stream, a));
-    const int64_t C = ceil_div(N, chunk);
-    cudaError_t e = launch_norms(a, geom(N, chunk), C, norms, (cudaStream_t)stream);
+    cudaError_t e = launch_norms(a, ugeom(N, chunk), norms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "chunk_norms launch");
     return ok();
 }
@@ -283,7 +297,13 @@ fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
             return fail(FC_ERR_INVALID_ARG, "N and chunk do not give C chunks");
     }
     TRY(bind_device(stream, norms));
-    cudaError_t e = launch_select(nullptr, 1, const_cast<float *>(norms), C, k,
+    UnitGeom G;
+    G.N = N;
+    G.cs = chunk;
+    G.C = C;
+    G.U = 1;
+    G.units = C;
+    cudaError_t e = launch_select(G, nullptr, nullptr, const_cast<float *>(norms), k,
                                   idx, mask, nullptr, threshold, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "chunk_select launch");
     if (packed) {
@@ -335,9 +355,7 @@ fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
 size_t fc_step_workspace_size(int64_t N, int64_t chunk)
 {
     if (N < 1 || chunk < 1) return 0;
-    const int64_t C = ceil_div(N, chunk);
-    const int64_t P = ceil_div(chunk, FC_TILE);
-    return ws_partials_bytes(C, P) + align256((size_t)C * sizeof(int32_t));
+    return ws_layout(N, chunk).total;
 }
 
 static fc_status check_ws(int64_t N, int64_t chunk, void *ws, size_t bytes)
@@ -367,18 +385,18 @@ fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
     TRY(bind_device(stream, a));
     const float u = (float)(1.0 / ((double)loss_scale * (double)W));
-    const TileGeom G = geom(N, chunk);
-    const int64_t tiles = ceil_div(N, chunk) * G.P;
-    double *partials = (double *)workspace;
+    const UnitGeom G = ugeom(N, chunk);
+    const WsLayout wl = ws_layout(N, chunk);
+    float *partials = (float *)((char *)workspace + wl.partials);
     cudaError_t e;
     if (fits_small(W, L)) {
         TableS tab;
         fill_table(tab, grads, W, L, sizes);
-        e = launch_reduce(tab, G, tiles, u, residual, a, partials, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream);
     } else {
         static thread_local TableL tab;
         fill_table(tab, grads, W, L, sizes);
-        e = launch_reduce(tab, G, tiles, u, residual, a, partials, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream);
     }
     if (e != cudaSuccess) return cuda_fail(e, "step_reduce launch");
     return ok();
@@ -395,11 +413,12 @@ fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
     TRY(check_f32(norms, "norms", false));
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
     TRY(bind_device(stream, norms));
-    const int64_t P = ceil_div(chunk, FC_TILE);
-    double *partials = (double *)workspace;
-    int32_t *slot = (int32_t *)((char *)workspace + ws_partials_bytes(C, P));
-    cudaError_t e = launch_select(partials, P, norms, C, k, idx, mask, slot,
-                                  threshold, (cudaStream_t)stream);
+    const WsLayout wl = ws_layout(N, chunk);
+    const float *partials = (const float *)((const char *)workspace + wl.partials);
+    unsigned *done = (unsigned *)((char *)workspace + wl.counters);
+    int32_t *slot = (int32_t *)((char *)workspace + wl.slot);
+    cudaError_t e = launch_select(ugeom(N, chunk), partials, done, norms, k, idx,
+                                  mask, slot, threshold, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "step_select launch");
     return ok();
 }
@@ -417,7 +436,7 @@ fc_status fc_step_update(const float *a, int64_t N, int64_t chunk, float lr,
     TRY(bind_device(stream, a));
     const TileGeom G = geom(N, chunk);
     const int64_t C = ceil_div(N, chunk);
-    const int32_t *slot = (const int32_t *)((char *)workspace + ws_partials_bytes(C, G.P));
+    const int32_t *slot = (const int32_t *)((char *)workspace + ws_layout(N, chunk).slot);
     cudaError_t e = launch_update(G, C * G.P, a, mask, slot, packed, lr,
                                   momentum, residual, velocity, weights,
                                   (__half *)weights_fp16, a == residual,

@@ -1,16 +1,21 @@
 // Device-side building blocks shared by the engine's kernels.
 //
-// Layout conventions (all kernels):
+// Layout conventions:
 //  * The fused vector has N elements; layer l occupies [off[l], off[l+1]).
 //  * Chunks of `cs` elements split the fused vector (the last may be short).
-//  * Work is cut into tiles of at most FC_TILE elements that never straddle a
-//    chunk: chunk c owns tiles c*P .. c*P+P-1 with P = ceil(cs / FC_TILE);
-//    tile j of chunk c covers [c*cs + j*FC_TILE, min(+FC_TILE, c*cs+cs, N)).
-//  * Inside a tile, thread t of a 256-thread block handles the 8-element
-//    groups [8g, 8g+8) (absolute fused index, clipped to the tile) with
-//    g = floor(lo/8) + t + 256*r.  The sum of squares of a tile is formed the
-//    same way by every kernel that needs it, so the norms are bitwise
-//    reproducible across the pipeline and the standalone calls.
+//  * Reduction and norms work on units of at most FC_UNIT = 256 elements that
+//    never straddle a chunk: chunk c owns units c*U .. with U = ceil(cs/256);
+//    unit j of chunk c covers [c*cs + 256j, min(+256, c*cs+cs, N)).  One warp
+//    handles one unit: lane t takes the 8-element groups [8g, 8g+8) (absolute
+//    fused index, clipped to the unit) with g = floor(lo/8) + t + 32r.
+//  * The sum of squares of a unit is the warp butterfly of the lanes' sums of
+//    their groups (each group summed pairwise).  A chunk's sum of squares is
+//    formed from its unit sums in binary64 in one fixed order: lane t adds the
+//    units j = t, t+32, t+64, ... in turn, then a butterfly over the 32 lanes.
+//    Every kernel that needs norms follows this order, so the norms are
+//    bitwise identical across the fused pipeline and the standalone calls.
+//  * The update works on tiles of at most FC_TILE = 2048 elements that never
+//    straddle a chunk (chunk c owns tiles c*P .. with P = ceil(cs/2048)).
 #pragma once
 
 #include <cuda_fp16.h>
@@ -18,8 +23,8 @@
 #include <stdint.h>
 
 #define FC_TILE 2048
+#define FC_UNIT 256
 #define FC_BLOCK 256
-#define FC_GROUP 8
 
 namespace fc {
 
@@ -53,6 +58,31 @@ __device__ __forceinline__ bool tile_range(const TileGeom &G, int64_t t,
     hi_nominal = lo + FC_TILE < cend ? lo + FC_TILE : cend;
     hi = hi_nominal < G.N ? hi_nominal : G.N;
     return lo < hi;
+}
+
+struct UnitGeom {
+    int64_t N;      // elements
+    int64_t cs;     // chunk size
+    int64_t U;      // units per (full) chunk
+    int64_t C;      // chunks
+    int64_t units;  // total units: (C-1)*U + units of the last chunk
+};
+
+__device__ __forceinline__ void unit_range(const UnitGeom &G, int64_t u,
+                                           int64_t &c, int64_t &lo,
+                                           int64_t &hi)
+{
+    c = u / G.U;
+    const int64_t j = u - c * G.U;
+    const int64_t cend = c * G.cs + G.cs < G.N ? c * G.cs + G.cs : G.N;
+    lo = c * G.cs + j * FC_UNIT;
+    hi = lo + FC_UNIT < cend ? lo + FC_UNIT : cend;
+}
+
+// Number of units of chunk c.
+__device__ __forceinline__ int64_t units_of_chunk(const UnitGeom &G, int64_t c)
+{
+    return c + 1 < G.C ? G.U : G.units - c * G.U;
 }
 
 // Smallest l with off[l+1] > f (skips empty layers).
@@ -212,24 +242,21 @@ __device__ __forceinline__ float group_sumsq(const float (&v)[8])
                      __fadd_rn(__fadd_rn(q[4], q[5]), __fadd_rn(q[6], q[7])));
 }
 
-// Tile total of the per-thread sums: butterfly within each warp (every lane
-// ends with the same value), then the 8 warp sums added in order in fp64.
-// Must be called by all FC_BLOCK threads; the result is valid in thread 0.
-__device__ __forceinline__ double block_tile_sumsq(float tss, float *red8)
+// Butterfly sums over the 32 lanes: every lane ends with the same value.
+__device__ __forceinline__ float warp_sum_f32(float x)
 {
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1)
-        tss = __fadd_rn(tss, __shfl_xor_sync(0xffffffffu, tss, o));
-    const int warp = threadIdx.x >> 5;
-    __syncthreads();  // red8 may still be read from the previous tile
-    if ((threadIdx.x & 31) == 0) red8[warp] = tss;
-    __syncthreads();
-    double d = 0.0;
-    if (threadIdx.x == 0) {
+        x = __fadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
+}
+
+__device__ __forceinline__ double warp_sum_f64(double x)
+{
 #pragma unroll
-        for (int w = 0; w < FC_BLOCK / 32; ++w) d = __dadd_rn(d, (double)red8[w]);
-    }
-    return d;
+    for (int o = 16; o > 0; o >>= 1)
+        x = __dadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
+    return x;
 }
 
 __device__ __forceinline__ float norm_from_sumsq(double ss)

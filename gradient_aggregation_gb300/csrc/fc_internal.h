@@ -13,24 +13,28 @@ template <class Tab>
 bool fill_table(Tab &t, const void *const *grads, int32_t W, int32_t L,
                 const int64_t *sizes);
 
-// Phase-1 / fc_tree_reduce kernel launch.  `partials` may be NULL.
+// Phase-1 / fc_tree_reduce kernel launch.  With partials != NULL the unit
+// sums of squares go to partials [G.units].
 template <class Tab>
-cudaError_t launch_reduce(const Tab &tab, const TileGeom &G, int64_t tiles,
-                          float u, const float *resid, float *out,
-                          double *partials, cudaStream_t s);
+cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
+                          const float *resid, float *out, float *partials,
+                          cudaStream_t s);
 
 template <class Tab>
 cudaError_t launch_pack(const Tab &tab, int64_t N, __half *fused,
                         cudaStream_t s);
 
-cudaError_t launch_norms(const float *a, const TileGeom &G, int64_t C,
-                         float *norms, cudaStream_t s);
+cudaError_t launch_norms(const float *a, const UnitGeom &G, float *norms,
+                         cudaStream_t s);
 
-// partials == NULL: norms are an input.  Otherwise norms are written from
-// the partials first.  slot may be NULL.
-cudaError_t launch_select(const double *partials, int64_t P, float *norms,
-                          int64_t C, int64_t k, int32_t *idx, uint8_t *mask,
-                          int32_t *slot, float *threshold, cudaStream_t s);
+// With partials == NULL, norms [C] is the input.  Otherwise the chunk
+// norms are first formed from the unit sums (partials [G.units]) by many
+// blocks and written to norms; `done` (zero on entry, zero on exit) counts
+// finished blocks and the last one selects.  slot may be NULL.
+cudaError_t launch_select(const UnitGeom &G, const float *partials,
+                          unsigned *done, float *norms, int64_t k,
+                          int32_t *idx, uint8_t *mask, int32_t *slot,
+                          float *threshold, cudaStream_t s);
 
 cudaError_t launch_gather(const float *a, int64_t N, int64_t cs, int64_t P,
                           const int32_t *idx, int64_t k, float *packed,

@@ -15,6 +15,8 @@
 // the registers, so the norms cost no extra pass.
 #include <stdio.h>
 
+#include <mutex>
+
 #include "fc_internal.h"
 
 namespace fc {
@@ -53,140 +55,172 @@ template bool fill_table<TableS>(TableS &, const void *const *, int32_t,
 template bool fill_table<TableL>(TableL &, const void *const *, int32_t,
                                  int32_t, const int64_t *);
 
+// SM count and resident blocks per SM are looked up once per (kernel,
+// device) and cached, so that later calls (for instance while a stream is
+// being captured into a CUDA graph) make no further runtime queries.
 int grid_for(const void *kernel, int block, size_t smem, int64_t work)
 {
-    int dev = 0, sms = 0, per_sm = 0;
+    struct Entry {
+        const void *kernel;
+        int dev, block, blocks;
+        size_t smem;
+    };
+    static std::mutex mu;
+    static Entry cache[256];
+    static int used = 0;
+    int dev = 0;
     cudaGetDevice(&dev);
-    cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block,
-                                                      smem) != cudaSuccess ||
-        per_sm < 1)
-        per_sm = 1;
-    if (sms < 1) sms = 1;
-    int64_t g = (int64_t)sms * per_sm;
+    int blocks = 0;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        for (int i = 0; i < used; ++i)
+            if (cache[i].kernel == kernel && cache[i].dev == dev &&
+                cache[i].block == block && cache[i].smem == smem) {
+                blocks = cache[i].blocks;
+                break;
+            }
+    }
+    if (blocks == 0) {
+        int sms = 0, per_sm = 0;
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, block,
+                                                          smem) != cudaSuccess ||
+            per_sm < 1)
+            per_sm = 1;
+        if (sms < 1) sms = 1;
+        blocks = sms * per_sm;
+        std::lock_guard<std::mutex> lock(mu);
+        if (used < 256) cache[used++] = Entry{kernel, dev, block, blocks, smem};
+    }
+    int64_t g = blocks;
     if (work < g) g = work;
     return g < 1 ? 1 : (int)g;
 }
 
 // ---- a2 kernel ------------------------------------------------------------------
+//
+// One warp per unit of 256 fused elements (see fc_common.cuh), no block-wide
+// synchronisation and no fences, so every warp streams independently.  With
+// `partials` given, the warp also writes the unit's sum of squares, which
+// the selection kernel turns into chunk norms.
 
 template <class Tab, int WT, int MAXH>
-__global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : 2)
-    k_reduce(const __grid_constant__ Tab tab, const TileGeom G,
-             const int64_t tiles, const float u, const float *resid,
-             float *out, double *partials)
+__global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0 && WT <= 16) ? 3 : 2))
+    k_reduce(const __grid_constant__ Tab tab, const UnitGeom G, const float u,
+             const float *resid, float *out, float *partials)
 {
-    __shared__ float red8[FC_BLOCK / 32];
     const uint64_t pol = policy_evict_first();
     const int W = WT > 0 ? WT : tab.W;
     const int L = tab.L;
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
 
-    for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
-        int64_t lo, hi, c, hin;
-        const bool any = tile_range(G, t, lo, hi, c, hin);
+    for (int64_t un = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+         un < G.units; un += nwarps) {
+        int64_t c, lo, hi;
+        unit_range(G, un, c, lo, hi);
         float tss = 0.f;
-        if (any) {
-            const int64_t g1 = (hi + 7) >> 3;
-            for (int64_t g = (lo >> 3) + threadIdx.x; g < g1; g += FC_BLOCK) {
-                const int64_t f0 = g << 3;
-                float a[8];
-                const bool full = (f0 >= lo) && (f0 + 8 <= hi);
-                int l = find_layer(tab, f0 > lo ? f0 : lo);
-                if (full && f0 + 8 <= tab.off[l + 1] &&
-                    ((tab.vec[l >> 5] >> (l & 31)) & 1u)) {
-                    // vector path: 8 consecutive elements of one layer
-                    const int64_t j = f0 - tab.off[l];
-                    tree_sum<WT, MAXH, 8>(
-                        W,
-                        [&](int w, float(&x)[8]) {
-                            unpack8(ld_stream16(tab.ptr[w * L + l] + j, pol), x);
-                        },
-                        a);
-                    float r[8];
-                    if (resid) {
-                        const float4 r0 = __ldcs(reinterpret_cast<const float4 *>(resid + f0));
-                        const float4 r1 = __ldcs(reinterpret_cast<const float4 *>(resid + f0 + 4));
-                        r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
-                        r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
-                    }
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        a[e] = __fmul_rn(a[e], u);
-                        if (resid) a[e] = __fadd_rn(a[e], r[e]);
-                    }
-                    reinterpret_cast<float4 *>(out + f0)[0] = make_float4(a[0], a[1], a[2], a[3]);
-                    reinterpret_cast<float4 *>(out + f0)[1] = make_float4(a[4], a[5], a[6], a[7]);
-                } else {
-                    // scalar path: group clipped by the tile, crossing a
-                    // layer boundary, or a misaligned layer
-#pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        const int64_t f = f0 + e;
-                        if (f < lo || f >= hi) {
-                            a[e] = 0.f;
-                            continue;
-                        }
-                        while (tab.off[l + 1] <= f) ++l;
-                        const int64_t j = f - tab.off[l];
-                        float s1[1];
-                        tree_sum<WT, MAXH, 1>(
-                            W,
-                            [&](int w, float(&x)[1]) {
-                                x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
-                            },
-                            s1);
-                        float v = __fmul_rn(s1[0], u);
-                        if (resid) v = __fadd_rn(v, __ldcs(resid + f));
-                        out[f] = v;
-                        a[e] = v;
-                    }
+        const int64_t g1 = (hi + 7) >> 3;
+        for (int64_t g = (lo >> 3) + lane; g < g1; g += 32) {
+            const int64_t f0 = g << 3;
+            float a[8];
+            const bool full = (f0 >= lo) && (f0 + 8 <= hi);
+            int l = find_layer(tab, f0 > lo ? f0 : lo);
+            if (full && f0 + 8 <= tab.off[l + 1] &&
+                ((tab.vec[l >> 5] >> (l & 31)) & 1u)) {
+                // vector path: 8 consecutive elements of one layer
+                const int64_t j = f0 - tab.off[l];
+                tree_sum<WT, MAXH, 8>(
+                    W,
+                    [&](int w, float(&x)[8]) {
+                        unpack8(ld_stream16(tab.ptr[w * L + l] + j, pol), x);
+                    },
+                    a);
+                float r[8];
+                if (resid) {
+                    const float4 r0 = __ldcs(reinterpret_cast<const float4 *>(resid + f0));
+                    const float4 r1 = __ldcs(reinterpret_cast<const float4 *>(resid + f0 + 4));
+                    r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
+                    r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
                 }
-                tss = __fadd_rn(tss, group_sumsq(a));
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    a[e] = __fmul_rn(a[e], u);
+                    if (resid) a[e] = __fadd_rn(a[e], r[e]);
+                }
+                reinterpret_cast<float4 *>(out + f0)[0] = make_float4(a[0], a[1], a[2], a[3]);
+                reinterpret_cast<float4 *>(out + f0)[1] = make_float4(a[4], a[5], a[6], a[7]);
+            } else {
+                // element path: group clipped by the unit, crossing a layer
+                // boundary, or a layer whose workers are not 16-byte aligned
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t f = f0 + e;
+                    if (f < lo || f >= hi) {
+                        a[e] = 0.f;
+                        continue;
+                    }
+                    while (tab.off[l + 1] <= f) ++l;
+                    const int64_t j = f - tab.off[l];
+                    float s1[1];
+                    tree_sum<WT, MAXH, 1>(
+                        W,
+                        [&](int w, float(&x)[1]) {
+                            x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
+                        },
+                        s1);
+                    float v = __fmul_rn(s1[0], u);
+                    if (resid) v = __fadd_rn(v, __ldcs(resid + f));
+                    out[f] = v;
+                    a[e] = v;
+                }
             }
+            tss = __fadd_rn(tss, group_sumsq(a));
         }
         if (partials) {
-            const double d = block_tile_sumsq(tss, red8);
-            if (threadIdx.x == 0) partials[t] = d;
+            tss = warp_sum_f32(tss);
+            if (lane == 0) partials[un] = tss;
         }
     }
 }
 
 template <class Tab, int WT, int MAXH>
-static cudaError_t launch_reduce_w(const Tab &tab, const TileGeom &G,
-                                   int64_t tiles, float u, const float *resid,
-                                   float *out, double *partials, cudaStream_t s)
+static cudaError_t launch_reduce_w(const Tab &tab, const UnitGeom &G, float u,
+                                   const float *resid, float *out,
+                                   float *partials, cudaStream_t s)
 {
     auto kern = k_reduce<Tab, WT, MAXH>;
-    const int grid = grid_for((const void *)kern, FC_BLOCK, 0, tiles);
-    kern<<<grid, FC_BLOCK, 0, s>>>(tab, G, tiles, u, resid, out, partials);
+    const int64_t blocks_needed = (G.units + FC_BLOCK / 32 - 1) / (FC_BLOCK / 32);
+    const int grid = grid_for((const void *)kern, FC_BLOCK, 0, blocks_needed);
+    kern<<<grid, FC_BLOCK, 0, s>>>(tab, G, u, resid, out, partials);
     return cudaGetLastError();
 }
 
 template <class Tab>
-cudaError_t launch_reduce(const Tab &tab, const TileGeom &G, int64_t tiles,
-                          float u, const float *resid, float *out,
-                          double *partials, cudaStream_t s)
+cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
+                          const float *resid, float *out, float *partials,
+                          cudaStream_t s)
 {
     switch (tab.W) {
-    case 1: return launch_reduce_w<Tab, 1, 1>(tab, G, tiles, u, resid, out, partials, s);
-    case 2: return launch_reduce_w<Tab, 2, 2>(tab, G, tiles, u, resid, out, partials, s);
-    case 4: return launch_reduce_w<Tab, 4, 3>(tab, G, tiles, u, resid, out, partials, s);
-    case 8: return launch_reduce_w<Tab, 8, 4>(tab, G, tiles, u, resid, out, partials, s);
-    case 16: return launch_reduce_w<Tab, 16, 5>(tab, G, tiles, u, resid, out, partials, s);
-    case 32: return launch_reduce_w<Tab, 32, 6>(tab, G, tiles, u, resid, out, partials, s);
-    case 64: return launch_reduce_w<Tab, 64, 7>(tab, G, tiles, u, resid, out, partials, s);
+    case 1: return launch_reduce_w<Tab, 1, 1>(tab, G, u, resid, out, partials, s);
+    case 2: return launch_reduce_w<Tab, 2, 2>(tab, G, u, resid, out, partials, s);
+    case 4: return launch_reduce_w<Tab, 4, 3>(tab, G, u, resid, out, partials, s);
+    case 8: return launch_reduce_w<Tab, 8, 4>(tab, G, u, resid, out, partials, s);
+    case 16: return launch_reduce_w<Tab, 16, 5>(tab, G, u, resid, out, partials, s);
+    case 32: return launch_reduce_w<Tab, 32, 6>(tab, G, u, resid, out, partials, s);
+    case 64: return launch_reduce_w<Tab, 64, 7>(tab, G, u, resid, out, partials, s);
     default: break;
     }
-    if (tab.W < 32) return launch_reduce_w<Tab, 0, 5>(tab, G, tiles, u, resid, out, partials, s);
-    if (tab.W < 128) return launch_reduce_w<Tab, 0, 7>(tab, G, tiles, u, resid, out, partials, s);
-    return launch_reduce_w<Tab, 0, 12>(tab, G, tiles, u, resid, out, partials, s);
+    if (tab.W < 32) return launch_reduce_w<Tab, 0, 5>(tab, G, u, resid, out, partials, s);
+    if (tab.W < 128) return launch_reduce_w<Tab, 0, 7>(tab, G, u, resid, out, partials, s);
+    return launch_reduce_w<Tab, 0, 12>(tab, G, u, resid, out, partials, s);
 }
 
-template cudaError_t launch_reduce<TableS>(const TableS &, const TileGeom &,
-                                           int64_t, float, const float *,
-                                           float *, double *, cudaStream_t);
-template cudaError_t launch_reduce<TableL>(const TableL &, const TileGeom &,
-                                           int64_t, float, const float *,
-                                           float *, double *, cudaStream_t);
+template cudaError_t launch_reduce<TableS>(const TableS &, const UnitGeom &,
+                                           float, const float *, float *,
+                                           float *, cudaStream_t);
+template cudaError_t launch_reduce<TableL>(const TableL &, const UnitGeom &,
+                                           float, const float *, float *,
+                                           float *, cudaStream_t);
 
 }  // namespace fc

@@ -7,15 +7,16 @@
 // ascending) order.
 //
 // GB300 mapping:
-//  * norms: one block per chunk walks the chunk's tiles with the same
-//    thread/group mapping as the fused reduction kernel, so both produce the
-//    same bits;
-//  * select: C is at most a few thousand, so one 1024-thread block does a
-//    3-pass radix select (11/11/10 bits) on the norms' bit patterns
-//    (non-negative binary32 values order like their uint32 bits) with
-//    shared-memory histograms, then two block scans in index order give the
-//    tie-broken kept set, the ascending index list and each kept chunk's slot
-//    in the packed output;
+//  * norms: one block per chunk forms the chunk's unit sums with the same
+//    warp/lane mapping and the same binary64 order as the fused reduction
+//    kernel, so both produce the same bits;
+//  * select: in the pipeline, blocks of 32 warps first turn the reduction's
+//    unit sums into chunk norms (one warp per chunk, the fixed binary64
+//    order); the last block to finish then selects.  C is at most a few
+//    thousand, so one 1024-thread block holds the norms in shared memory and
+//    runs a 4-pass radix select (8 bits a pass) on their bit patterns, then
+//    one block scan in index order gives the tie-broken kept set, the
+//    ascending index list and each kept chunk's slot in the packed output;
 //  * gather: a grid-wide copy of the kept chunks into their slots.
 #include "fc_internal.h"
 
@@ -23,20 +24,31 @@ namespace fc {
 
 // ---- a3 ------------------------------------------------------------------------
 
+// One block of 8 warps per chunk.  Warp w forms the sums of the units
+// j = w, w+8, w+16, ... of the chunk exactly as the reduction kernel does, and
+// keeps four binary64 running sums, one per residue class j mod 32 it sees
+// (w, w+8, w+16, w+24), added in increasing j.  Those 32 class sums then go
+// through the same binary64 butterfly as the reduction kernel's chunk
+// finish, so both produce the same bits.
 __global__ void __launch_bounds__(FC_BLOCK)
-    k_norms(const float *__restrict__ a, const TileGeom G, const int64_t C,
+    k_norms(const float *__restrict__ a, const UnitGeom G,
             float *__restrict__ norms)
 {
-    __shared__ float red8[FC_BLOCK / 32];
-    for (int64_t c = blockIdx.x; c < C; c += gridDim.x) {
-        double acc = 0.0;
-        for (int64_t j = 0; j < G.P; ++j) {
-            int64_t lo, hi, cc, hin;
-            const bool any = tile_range(G, c * G.P + j, lo, hi, cc, hin);
-            float tss = 0.f;
-            if (any) {
+    __shared__ double res[32];
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    for (int64_t c = blockIdx.x; c < G.C; c += gridDim.x) {
+        const int64_t Uc = units_of_chunk(G, c);
+        double acc[4] = {0.0, 0.0, 0.0, 0.0};
+        for (int64_t base = 0; base < Uc; base += 32) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const int64_t j = base + warp + 8 * q;
+                if (j >= Uc) continue;
+                int64_t cc, lo, hi;
+                unit_range(G, c * G.U + j, cc, lo, hi);
+                float tss = 0.f;
                 const int64_t g1 = (hi + 7) >> 3;
-                for (int64_t g = (lo >> 3) + threadIdx.x; g < g1; g += FC_BLOCK) {
+                for (int64_t g = (lo >> 3) + lane; g < g1; g += 32) {
                     const int64_t f0 = g << 3;
                     float v[8];
                     if (f0 >= lo && f0 + 8 <= hi) {
@@ -53,19 +65,28 @@ __global__ void __launch_bounds__(FC_BLOCK)
                     }
                     tss = __fadd_rn(tss, group_sumsq(v));
                 }
+                tss = warp_sum_f32(tss);
+                acc[q] = __dadd_rn(acc[q], (double)tss);
             }
-            const double d = block_tile_sumsq(tss, red8);
-            if (threadIdx.x == 0) acc = __dadd_rn(acc, d);
         }
-        if (threadIdx.x == 0) norms[c] = norm_from_sumsq(acc);
+        if (lane == 0) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) res[warp + 8 * q] = acc[q];
+        }
+        __syncthreads();
+        if (warp == 0) {
+            const double ss = warp_sum_f64(res[lane]);
+            if (lane == 0) norms[c] = norm_from_sumsq(ss);
+        }
+        __syncthreads();
     }
 }
 
-cudaError_t launch_norms(const float *a, const TileGeom &G, int64_t C,
-                         float *norms, cudaStream_t s)
+cudaError_t launch_norms(const float *a, const UnitGeom &G, float *norms,
+                         cudaStream_t s)
 {
-    const int grid = grid_for((const void *)k_norms, FC_BLOCK, 0, C);
-    k_norms<<<grid, FC_BLOCK, 0, s>>>(a, G, C, norms);
+    const int grid = grid_for((const void *)k_norms, FC_BLOCK, 0, G.C);
+    k_norms<<<grid, FC_BLOCK, 0, s>>>(a, G, norms);
     return cudaGetLastError();
 }
 
@@ -73,141 +94,195 @@ cudaError_t launch_norms(const float *a, const TileGeom &G, int64_t C,
 
 #define SEL_THREADS 1024
 #define SEL_ITEMS 4
+#define SEL_SMEM_KEYS 11264
 
-// Exclusive prefix sum over the 1024 threads; *total gets the block sum.
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t x, uint32_t *sw,
-                                                    uint32_t &total)
+// Exclusive prefix sum over the 1024 threads; `total` gets the block sum.
+__device__ __forceinline__ uint64_t block_excl_scan64(uint64_t x, uint64_t *sw,
+                                                      uint64_t &total)
 {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t inc = x;
+    uint64_t inc = x;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+        const uint64_t y = __shfl_up_sync(0xffffffffu, inc, o);
         if (lane >= o) inc += y;
     }
     __syncthreads();  // sw may still be read by the previous scan
     if (lane == 31) sw[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        uint32_t t = sw[lane];
+        uint64_t t = sw[lane];
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xffffffffu, t, o);
+            const uint64_t y = __shfl_up_sync(0xffffffffu, t, o);
             if (lane >= o) t += y;
         }
         sw[lane] = t;
     }
     __syncthreads();
     total = sw[31];
-    return (warp ? sw[warp - 1] : 0u) + inc - x;
+    return (warp ? sw[warp - 1] : 0ull) + inc - x;
 }
 
+// Chunk norm from the unit sums, in the fixed order (see fc_common.cuh):
+// lane t adds units t, t+32, ... in binary64, then a binary64 butterfly.
+// Called by a whole warp; the result is valid in every lane.
+__device__ __forceinline__ float chunk_norm_from_units(const UnitGeom &G,
+                                                       const float *partials,
+                                                       int64_t c, int lane)
+{
+    const int64_t Uc = units_of_chunk(G, c);
+    double ss = 0.0;
+    for (int64_t j = lane; j < Uc; j += 32)
+        ss = __dadd_rn(ss, (double)__ldcg(partials + c * G.U + j));
+    return norm_from_sumsq(warp_sum_f64(ss));
+}
+
+// Selection kernel.  With partials != NULL every block first turns the unit
+// sums of 32 chunks (one per warp) into norms; the block that finishes last
+// (a count of finished blocks in `done`, reset by that block) then runs the
+// selection.  With partials == NULL there is one block and the norms are an
+// input.  No block ever waits for another.
+//
+// Selection: the norms' bit patterns (non-negative binary32 values order like
+// their uint32 patterns) go to shared memory; four radix passes of 8 bits
+// find the pattern tau of the k-th largest norm and how many chunks equal to
+// tau are kept (`need`: the lowest-indexed ones); one block scan in index
+// order then places every kept chunk: its slot is the number of kept chunks
+// before it = (#greater before it) + min(#equal before it, need).
 __global__ void __launch_bounds__(SEL_THREADS)
-    k_select(const double *__restrict__ partials, const int64_t P,
-             float *norms, const int64_t C, const int64_t k,
+    k_select(const UnitGeom G, const float *__restrict__ partials,
+             unsigned *__restrict__ done, float *norms, const int64_t k,
              int32_t *__restrict__ idx, uint8_t *__restrict__ mask,
              int32_t *__restrict__ slot, float *__restrict__ threshold)
 {
-    __shared__ uint32_t hist[2048];
-    __shared__ uint32_t sw[32];
-    __shared__ uint32_t s_digit, s_rem;
+    __shared__ uint32_t skeys[SEL_SMEM_KEYS];
+    __shared__ uint32_t hist[256];
+    __shared__ uint64_t sw[32];
+    __shared__ uint32_t s_digit, s_rem, s_last;
     const int tid = threadIdx.x;
+    const int64_t C = G.C;
 
-    // finish the norms from the per-tile partial sums (same order as k_norms)
     if (partials) {
-        for (int64_t c = tid; c < C; c += SEL_THREADS) {
-            double ss = 0.0;
-            for (int64_t j = 0; j < P; ++j) ss = __dadd_rn(ss, partials[c * P + j]);
-            norms[c] = norm_from_sumsq(ss);
+        const int lane = tid & 31, warp = tid >> 5;
+        for (int64_t c = (int64_t)blockIdx.x * 32 + warp; c < C;
+             c += (int64_t)gridDim.x * 32) {
+            const float n = chunk_norm_from_units(G, partials, c, lane);
+            if (lane == 0) norms[c] = n;
+        }
+        __threadfence();  // publish this block's norms before counting it
+        __syncthreads();
+        if (tid == 0) {
+            const unsigned seen = atomicAdd(done, 1u);
+            s_last = seen == gridDim.x - 1 ? 1u : 0u;
         }
         __syncthreads();
+        if (!s_last) return;
+        __threadfence();
+        if (tid == 0) *done = 0u;  // ready for the next call
     }
 
-    // radix select of the k-th largest key
+    const bool in_smem = C <= SEL_SMEM_KEYS;
+    if (in_smem) {
+        for (int64_t c = tid; c < C; c += SEL_THREADS) skeys[c] = __float_as_uint(__ldcg(norms + c));
+        __syncthreads();
+    }
+    auto key_at = [&](int64_t c) -> uint32_t {
+        return in_smem ? skeys[c] : __float_as_uint(__ldcg(norms + c));
+    };
+
     uint32_t prefix = 0, rem = (uint32_t)k;
 #pragma unroll 1
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int bits = pass == 2 ? 10 : 11;
-        const int nb = 1 << bits;
-        for (int b = tid; b < 2048; b += SEL_THREADS) hist[b] = 0;
+    for (int pass = 0; pass < 4; ++pass) {
+        const int shift = 24 - 8 * pass;
+        if (tid < 256) hist[tid] = 0;
         __syncthreads();
         for (int64_t c = tid; c < C; c += SEL_THREADS) {
-            const uint32_t key = __float_as_uint(norms[c]);
-            if (pass == 0 || (key >> (shift + bits)) == prefix)
-                atomicAdd(&hist[(key >> shift) & (nb - 1)], 1u);
+            const uint32_t key = key_at(c);
+            if (pass == 0 || (key >> (shift + 8)) == prefix)
+                atomicAdd(&hist[(key >> shift) & 255u], 1u);
         }
         __syncthreads();
-        const int per = nb / SEL_THREADS;  // 2 or 1 bins per thread, descending
-        uint32_t local = 0;
-        for (int i = 0; i < per; ++i) local += hist[nb - 1 - (per * tid + i)];
-        uint32_t tot;
-        uint32_t above = block_excl_scan(local, sw, tot);
-        for (int i = 0; i < per; ++i) {
-            const int b = nb - 1 - (per * tid + i);
-            const uint32_t h = hist[b];
-            if (above < rem && rem <= above + h) {
-                s_digit = (uint32_t)b;
-                s_rem = rem - above;
+        if (tid < 32) {
+            // lane t owns bins 255-8t .. 248-8t, from the top down
+            uint32_t h[8], local = 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                h[i] = hist[255 - 8 * tid - i];
+                local += h[i];
             }
-            above += h;
+            uint32_t inc = local;
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+                if (tid >= o) inc += y;
+            }
+            uint32_t above = inc - local;  // keys in higher bins
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                if (above < rem && rem <= above + h[i]) {
+                    s_digit = (uint32_t)(255 - 8 * tid - i);
+                    s_rem = rem - above;
+                }
+                above += h[i];
+            }
         }
         __syncthreads();
-        prefix = (prefix << bits) | s_digit;
+        prefix = (prefix << 8) | s_digit;
         rem = s_rem;
-        __syncthreads();
     }
     const uint32_t tau = prefix;  // bit pattern of the k-th largest norm
-    const uint32_t need = rem;    // how many chunks equal to tau are kept
+    const uint32_t need = rem;    // chunks equal to tau that are kept
 
-    // compaction in index order: ties kept from the lowest index up
-    uint32_t eq_carry = 0, kept_carry = 0;
+    uint32_t gt_carry = 0, eq_carry = 0;
     for (int64_t base = 0; base < C; base += SEL_THREADS * SEL_ITEMS) {
         uint32_t key[SEL_ITEMS];
-        bool valid[SEL_ITEMS], kept[SEL_ITEMS];
-        uint32_t neq = 0;
+        uint32_t ngt = 0, neq = 0;
 #pragma unroll
         for (int i = 0; i < SEL_ITEMS; ++i) {
             const int64_t c = base + (int64_t)tid * SEL_ITEMS + i;
-            valid[i] = c < C;
-            key[i] = valid[i] ? __float_as_uint(norms[c]) : 0u;
-            neq += (valid[i] && key[i] == tau) ? 1u : 0u;
-        }
-        uint32_t eq_tot;
-        uint32_t eqr = block_excl_scan(neq, sw, eq_tot) + eq_carry;
-        uint32_t nk = 0;
-#pragma unroll
-        for (int i = 0; i < SEL_ITEMS; ++i) {
-            const bool eq = valid[i] && key[i] == tau;
-            kept[i] = valid[i] && (key[i] > tau || (eq && eqr < need));
-            eqr += eq ? 1u : 0u;
-            nk += kept[i] ? 1u : 0u;
-        }
-        uint32_t k_tot;
-        uint32_t pos = block_excl_scan(nk, sw, k_tot) + kept_carry;
-#pragma unroll
-        for (int i = 0; i < SEL_ITEMS; ++i) {
-            const int64_t c = base + (int64_t)tid * SEL_ITEMS + i;
-            if (!valid[i]) continue;
-            mask[c] = kept[i] ? 1 : 0;
-            if (slot) slot[c] = kept[i] ? (int32_t)pos : -1;
-            if (kept[i]) {
-                if (pos < (uint32_t)k) idx[pos] = (int32_t)c;  // always true
-                ++pos;
+            key[i] = c < C ? key_at(c) : 0u;
+            if (c < C) {
+                ngt += key[i] > tau ? 1u : 0u;
+                neq += key[i] == tau ? 1u : 0u;
             }
         }
-        eq_carry += eq_tot;
-        kept_carry += k_tot;
+        uint64_t tot;
+        const uint64_t ex = block_excl_scan64(((uint64_t)neq << 32) | ngt, sw, tot);
+        uint32_t gtb = (uint32_t)ex + gt_carry;
+        uint32_t eqb = (uint32_t)(ex >> 32) + eq_carry;
+#pragma unroll
+        for (int i = 0; i < SEL_ITEMS; ++i) {
+            const int64_t c = base + (int64_t)tid * SEL_ITEMS + i;
+            if (c >= C) break;
+            const bool gt = key[i] > tau, eq = key[i] == tau;
+            const bool kept = gt || (eq && eqb < need);
+            const uint32_t pos = gtb + (eqb < need ? eqb : need);
+            mask[c] = kept ? 1 : 0;
+            if (slot) slot[c] = kept ? (int32_t)pos : -1;
+            if (kept && pos < (uint32_t)k) idx[pos] = (int32_t)c;
+            gtb += gt ? 1u : 0u;
+            eqb += eq ? 1u : 0u;
+        }
+        gt_carry += (uint32_t)tot;
+        eq_carry += (uint32_t)(tot >> 32);
     }
     if (tid == 0) threshold[0] = __uint_as_float(tau);
 }
 
-cudaError_t launch_select(const double *partials, int64_t P, float *norms,
-                          int64_t C, int64_t k, int32_t *idx, uint8_t *mask,
-                          int32_t *slot, float *threshold, cudaStream_t s)
+cudaError_t launch_select(const UnitGeom &G, const float *partials,
+                          unsigned *done, float *norms, int64_t k,
+                          int32_t *idx, uint8_t *mask, int32_t *slot,
+                          float *threshold, cudaStream_t s)
 {
-    k_select<<<1, SEL_THREADS, 0, s>>>(partials, P, norms, C, k, idx, mask,
-                                       slot, threshold);
+    int64_t blocks = 1;
+    if (partials) {
+        blocks = (G.C + 31) / 32;
+        const int cap = grid_for((const void *)k_select, SEL_THREADS, 0, blocks);
+        if (blocks > cap) blocks = cap;  // all blocks resident: no queueing
+    }
+    k_select<<<(int)blocks, SEL_THREADS, 0, s>>>(G, partials, done, norms, k,
+                                                 idx, mask, slot, threshold);
     return cudaGetLastError();
 }
 

@@ -279,7 +279,8 @@ class Engine:
         self.packed = (torch.empty(self.k * self.chunk, dtype=torch.float32, device=dev)
                        if want_packed else None)
         self.threshold = torch.empty(1, dtype=torch.float32, device=dev)
-        self.workspace = torch.empty(fc_step_workspace_size(self.N, self.chunk),
+        # zero-filled once; the pipeline keeps its counters at zero
+        self.workspace = torch.zeros(fc_step_workspace_size(self.N, self.chunk),
                                      dtype=torch.uint8, device=dev)
 
     def step(self, grads, stream=None) -> None:

@@ -45,9 +45,10 @@
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *    are asynchronous and stream-ordered; a returned FC_OK means the
  *    arguments were valid and the kernels were launched, not that they
- *    finished.  No call synchronises, so sequences can be captured in a
- *    CUDA graph.  The device is the one that owns `stream` (or, for the
- *    NULL stream, the first device pointer argument).
+ *    finished.  No call synchronises or queries the stream, so sequences
+ *    can be captured in a CUDA graph (after one call outside capture has
+ *    cached the launch configuration).  Kernels run on the device that owns
+ *    the call's main device buffer (the output for most calls).
  *  - fp32 arrays and fp16 outputs must be 16-byte aligned; fp16 gradient
  *    inputs must be 2-byte aligned (16-byte aligned ones take the vector
  *    path).  Otherwise FC_ERR_ALIGNMENT.
@@ -143,10 +144,10 @@ FC_API fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
 /* ---- a3: chunk norms ---------------------------------------------------------- */
 
 /* norms[c] = sqrt(sum_{i in chunk c} a[i]^2), c < C = fc_num_chunks(N, chunk).
- * Squares and partial sums in fp32 over groups of at most 256 elements
- * (pairs of 8, then a warp butterfly), those partials summed in fp64; the
- * relative error is below 6e-7.  Deterministic: the same inputs give the
- * same bits, and the same bits as the norms fc_step_select reports.
+ * Squares and partial sums in fp32 over units of at most 256 elements
+ * (pairs of 8, then a warp butterfly), the unit sums added in fp64 in a
+ * fixed order; the relative error is below 6e-7.  Deterministic: the same
+ * inputs give the same bits, and the same bits as fc_step_reduce.
  *  a      device fp32 [N].
  *  norms  device fp32 [C] output. */
 FC_API fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
@@ -189,45 +190,50 @@ FC_API fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
 /* ---- the fused pipeline (a1..a5 without materialising the fused buffer) ---- */
 
 /* Bytes of scratch the pipeline needs for N elements in chunks of `chunk`
- * (per-tile partial sums of squares and the kept-slot map); 0 on bad
- * arguments. */
+ * (per-unit sums of squares, a count of finished selection blocks and the
+ * kept-slot map); 0 on bad arguments.  The workspace must be zero-filled
+ * before its first use with a given (N, chunk), e.g. by cudaMemsetAsync;
+ * every pipeline step leaves the count at zero again. */
 FC_API size_t fc_step_workspace_size(int64_t N, int64_t chunk);
 
-/* Phase 1 of the pipeline: a2 + the partial sums of a3, reading every
- * worker's layer tensors in place through the layout of a1 (the fused buffer
- * itself is never written):
+/* Phase 1 of the pipeline: a2 and the per-unit sums of squares of a3,
+ * reading every worker's layer tensors in place through the layout of a1
+ * (the fused buffer itself is never written):
  *   a[f] = tree_w(grads[w*L + l][f - offsets[l]]) * u + residual[f]
- * for every fused index f in layer l.  Results are bit-identical to
+ * for every fused index f in layer l.  `a` is bit-identical to
  * fc_fuse_pack + fc_tree_reduce.
  *  grads, W, L, sizes  as for fc_fuse_pack.
  *  residual  device fp32 [N] or NULL.
  *  a         device fp32 [N] output; may alias residual (in place).
- *  workspace device, fc_step_workspace_size(N, chunk) bytes, 256-aligned. */
+ *  workspace device, fc_step_workspace_size(N, chunk) bytes, 256-aligned,
+ *            zero-filled before first use. */
 FC_API fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
-                         const int64_t *sizes, float loss_scale,
-                         int64_t chunk, const float *residual, float *a,
-                         void *workspace, size_t workspace_bytes,
-                         void *stream);
+                                const int64_t *sizes, float loss_scale,
+                                int64_t chunk, const float *residual, float *a,
+                                void *workspace, size_t workspace_bytes,
+                                void *stream);
 
-/* Phase 2: finishes the chunk norms from the phase-1 partials (bitwise the
- * same as fc_chunk_norms on a) and selects the top k chunks exactly as
- * fc_chunk_select does.  norms [C], idx [k], mask [C], threshold [1] are
- * device outputs; the kept-slot map for phase 3 goes to the workspace. */
-FC_API fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
-                         int32_t *idx, uint8_t *mask, float *threshold,
-                         void *workspace, size_t workspace_bytes,
-                         void *stream);
+/* Phase 2: finishes the chunk norms from phase 1's unit sums (norms [C],
+ * device output, bitwise the same as fc_chunk_norms on a) and selects the
+ * top k chunks exactly as fc_chunk_select does (idx [k], mask [C],
+ * threshold [1] are device outputs); each kept chunk's slot in the packed
+ * output goes to the workspace for phase 3. */
+FC_API fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k,
+                                float *norms, int32_t *idx, uint8_t *mask,
+                                float *threshold, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /* Phase 3: the a5 update of fc_residual_sgd_update, which also writes the
  * kept chunks into `packed` (device fp32 [k*chunk] or NULL, laid out as in
- * fc_chunk_select).  When a == residual (in place), unkept elements already
- * hold their new residual and are neither read nor rewritten. */
-FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk, float lr,
-                         float momentum, float *residual, float *velocity,
-                         float *weights, void *weights_fp16,
-                         const uint8_t *mask, float *packed,
-                         void *workspace, size_t workspace_bytes,
-                         void *stream);
+ * fc_chunk_select).  `mask` must be the one phase 2 wrote.  When
+ * a == residual (in place), unkept elements already hold their new residual
+ * and are neither read nor rewritten. */
+FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk,
+                                float lr, float momentum, float *residual,
+                                float *velocity, float *weights,
+                                void *weights_fp16, const uint8_t *mask,
+                                float *packed, void *workspace,
+                                size_t workspace_bytes, void *stream);
 
 /* Phases 1-3 in one call on one stream (three kernel launches). */
 FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,

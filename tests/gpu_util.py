@@ -52,7 +52,7 @@ class GpuRun:
         self.packed = (torch.empty(self.k * wl.chunk, dtype=torch.float32, device=device)
                        if want_packed else None)
         self.threshold = torch.empty(1, dtype=torch.float32, device=device)
-        self.ws = torch.empty(fc.fc_step_workspace_size(N, wl.chunk), dtype=torch.uint8,
+        self.ws = torch.zeros(fc.fc_step_workspace_size(N, wl.chunk), dtype=torch.uint8,
                               device=device)
         self.fused = (torch.empty(W * N, dtype=torch.float16, device=device)
                       if path == "separate" else None)

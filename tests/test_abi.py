@@ -112,6 +112,7 @@ def test_argument_errors_return_before_any_device_work(fc_lib):
     assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, fake, None, 0, None) == fc.FC_ERR_WORKSPACE
     assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, fake, fake, 1, None) == fc.FC_ERR_WORKSPACE
     assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, fake, fake + 16, 10 ** 6, None) == fc.FC_ERR_ALIGNMENT
+    assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, None, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
     assert L.fc_step_select(16, 4, 9, fake, fake, fake, fake, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
     assert L.fc_step_update(fake, 16, 4, 0.1, 0.9, fake, fake, fake, None, fake, fake + 4, fake, 10 ** 6, None) == fc.FC_ERR_ALIGNMENT
     assert L.fc_step(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, 5, 0.1, 0.9, fake, fake, fake, fake,
