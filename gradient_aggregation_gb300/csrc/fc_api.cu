@@ -475,3 +475,20 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
 }
 
 }  // extern "C"
+
+// ---- helpers for other translation units of the library ----------------------
+
+namespace fc {
+
+fc_status set_error(fc_status st, const char *msg)
+{
+    snprintf(g_err, sizeof(g_err), "%s", msg);
+    return st;
+}
+
+size_t step_ws_counter_offset(int64_t N, int64_t chunk)
+{
+    return ws_layout(N, chunk).counters;
+}
+
+}  // namespace fc

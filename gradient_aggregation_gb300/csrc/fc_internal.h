@@ -4,6 +4,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include "fc.h"
 #include "fc_common.cuh"
 
 namespace fc {
@@ -45,6 +46,13 @@ cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           float *packed, float lr, float mu, float *r,
                           float *v, float *w, __half *w16, bool inplace,
                           cudaStream_t s);
+
+// Sets the calling thread's fc_last_error() message; returns st.
+fc_status set_error(fc_status st, const char *msg);
+
+// Byte offset, inside the pipeline workspace for (N, chunk), of the 256-byte
+// word block that must be zero before a step.
+size_t step_ws_counter_offset(int64_t N, int64_t chunk);
 
 // Blocks to launch for a grid-stride kernel: min(work, SMs * resident).
 int grid_for(const void *kernel, int block, size_t smem, int64_t work);

@@ -27,6 +27,7 @@ FC_ERR_CUDA = -4
 FC_ERR_LIMIT = -5
 FC_MAX_TABLE_PTRS = 3072
 FC_MAX_TABLE_LAYERS = 512
+FC_NOALLOC_WORKSPACE_BYTES = 4 << 20
 
 _lock = threading.Lock()
 _lib = None
@@ -50,6 +51,8 @@ _SIGS = {
     "fc_step_update": (ctypes.c_int, [_P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
     "fc_step": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _I64, _F32, _F32, _P, _P, _P,
                                _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "fc_step_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _I64, _F32, _F32, _P,
+                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
 }
 
 
@@ -241,6 +244,22 @@ def fc_step(grads, loss_scale: float, chunk: int, k: int, lr: float, momentum: f
                          _p(weights), _p(weights_fp16), _p(norms), _p(idx), _p(mask),
                          _p(packed), _p(threshold), _p(workspace), workspace.numel(),
                          _s(stream)))
+
+
+def fc_step_noalloc(grads, loss_scale: float, chunk: int, k: int, lr: float,
+                    momentum: float, residual: torch.Tensor, a: torch.Tensor,
+                    velocity: torch.Tensor, weights: torch.Tensor,
+                    weights_fp16: Optional[torch.Tensor], norms: torch.Tensor,
+                    idx: torch.Tensor, mask: torch.Tensor, packed: Optional[torch.Tensor],
+                    threshold: torch.Tensor, stream=None) -> None:
+    """fc_step with the library's built-in scratch array instead of a
+    caller workspace, for callers that cannot allocate device memory when
+    they step (see include/fc.h)."""
+    t = _table(grads)
+    _check(lib().fc_step_noalloc(t.ptrs, t.W, t.L, t.sizes_c, float(loss_scale), int(chunk),
+                                 int(k), float(lr), float(momentum), _p(residual), _p(a),
+                                 _p(velocity), _p(weights), _p(weights_fp16), _p(norms),
+                                 _p(idx), _p(mask), _p(packed), _p(threshold), _s(stream)))
 
 
 # ---- engine: device buffers for repeated steps ---------------------------------------

@@ -244,6 +244,41 @@ FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                   uint8_t *mask, float *packed, float *threshold,
                   void *workspace, size_t workspace_bytes, void *stream);
 
+/* ---- the pipeline without a caller workspace ---------------------------------- */
+
+/* Size of the scratch array built into the library for fc_step_noalloc. */
+#define FC_NOALLOC_WORKSPACE_BYTES (4u << 20)
+
+/* fc_step for callers that cannot allocate device memory when they step:
+ * code running while a stream is captured into a CUDA graph (cudaMalloc is
+ * not allowed then), frameworks whose pool allocator owns every device byte,
+ * and latency-critical loops that forbid allocation after start-up.  The
+ * pages have no counterpart to this call: it only changes where the scratch
+ * lives.
+ *
+ * Arguments and results are those of fc_step without the workspace.  The
+ * scratch is a FC_NOALLOC_WORKSPACE_BYTES (4 MiB) array inside the library,
+ * which every GPU that loads libfc holds until the process exits; a problem
+ * whose fc_step_workspace_size(N, chunk) exceeds it gets FC_ERR_LIMIT and
+ * nothing runs (4 MiB covers about 260 million elements in chunks that are
+ * multiples of 256).  The call allocates nothing: no cudaMalloc, no
+ * cudaFree, no allocating library routine.
+ *
+ * The first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress) with that device current and caches it; make that
+ * first call before capturing a stream.  Every call shares the one array per
+ * device: it clears the part that must start at zero on `stream` before its
+ * kernels, but two calls whose work overlaps on the GPU (different streams
+ * without ordering between them) race on the array and give wrong results. */
+FC_API fc_status fc_step_noalloc(const void *const *grads, int32_t W,
+                                 int32_t L, const int64_t *sizes,
+                                 float loss_scale, int64_t chunk, int64_t k,
+                                 float lr, float momentum, float *residual,
+                                 float *a, float *velocity, float *weights,
+                                 void *weights_fp16, float *norms,
+                                 int32_t *idx, uint8_t *mask, float *packed,
+                                 float *threshold, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

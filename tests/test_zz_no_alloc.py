@@ -1,0 +1,68 @@
+"""fc_step_noalloc: the fused pipeline for callers that cannot allocate
+device memory when they step (inside CUDA-graph capture, under a framework
+whose pool allocator owns all device memory, or in loops that forbid
+allocation after start-up).  It keeps its scratch in a fixed array built
+into libfc instead of a caller workspace.
+
+Its results must match fc_step with a caller workspace on the same inputs,
+over two calls in a row (the second call finds the array as the first one
+left it).  This file is collected last so that a failure here does not stop
+the other GPU tests.
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from gradient_aggregation_gb300 import fc, workload
+from tests.gpu_util import GpuRun, bits_equal, dev_grads, assert_close, RTOL_F32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(fc_lib):
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    yield
+
+
+def _noalloc_step(run, grads):
+    wl = run.wl
+    fc.fc_step_noalloc(grads, wl.loss_scale, wl.chunk, run.k, wl.lr, wl.momentum,
+                       run.residual, run.a, run.velocity, run.weights, run.w16, run.norms,
+                       run.idx, run.mask, run.packed, run.threshold)
+
+
+@pytest.mark.parametrize("name", ["tiny", "custom"])
+def test_noalloc_matches_workspace_pipeline_on_two_calls(name):
+    if name == "tiny":
+        wl = workload.get("tiny")
+    else:
+        wl = workload.custom(W=7, sizes=[5000, 33, 12000], chunk=1000, keep_percent=30,
+                             config_id=170, steps=2)
+    ref = GpuRun(wl, "pipeline")      # fc_step with a caller workspace
+    new = GpuRun(wl, "pipeline")      # same buffers, stepped by fc_step_noalloc
+    for step in range(2):
+        g = dev_grads(workload.all_grads(wl, step))
+        ref.step(g)
+        _noalloc_step(new, g)
+        a, b = ref.snapshot(), new.snapshot()
+        for key in ("a", "residual", "velocity", "weights", "norms", "threshold"):
+            assert_close(key, b[key], a[key], RTOL_F32)
+        for key in ("a", "residual", "velocity", "weights", "norms", "idx", "mask",
+                    "packed", "w16", "threshold"):
+            assert bits_equal(np.asarray(a[key]), np.asarray(b[key])), (step, key)
+
+
+def test_noalloc_rejects_problems_larger_than_its_array():
+    W, N = 2, 300_000_000            # needs more than 4 MiB of scratch
+    assert fc.fc_step_workspace_size(N, 256) > fc.FC_NOALLOC_WORKSPACE_BYTES
+    small = torch.zeros(16, dtype=torch.float16, device="cuda")
+    table = fc.PtrTable([[small], [small]])
+    table._sizes[0] = N              # the size check comes before any device work
+    out = torch.zeros(16, dtype=torch.float32, device="cuda")
+    with pytest.raises(fc.FcError) as e:
+        fc.fc_step_noalloc(table, 1.0, 256, 1, 0.1, 0.9, out, out, out, out, None, out,
+                           out.view(torch.int32), out.view(torch.uint8), None, out)
+    assert e.value.status == fc.FC_ERR_LIMIT
+    assert "built-in" in str(e.value)
