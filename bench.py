@@ -248,6 +248,23 @@ def traffic_from_profile(src_hash, wl):
         return None
 
 
+def max_over_ranks(x: float, device=None) -> float:
+    """The largest of every rank's x (identity without a process group)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return x
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def replica_value(world: int, step_bytes: int, steps: int, t_max: float) -> float:
+    """Whole-job worker-gradient GB/s: every replica processes step_bytes per
+    step; the job takes as long as the slowest rank."""
+    return world * step_bytes * steps / t_max / 1e9
+
+
 def run_gpu(args, wl, rank, world, local):
     import torch
     from gradient_aggregation_gb300 import fc
@@ -263,13 +280,8 @@ def run_gpu(args, wl, rank, world, local):
             import torch.distributed as dist
             dist.barrier()
 
-    def max_over_ranks(x):
-        if world == 1:
-            return x
-        import torch.distributed as dist
-        t = torch.tensor([x], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        return float(t.item())
+    def max_t(x):
+        return max_over_ranks(x, dev)
 
     fc.lib()
     W, N = wl.W, wl.N
@@ -297,8 +309,12 @@ def run_gpu(args, wl, rank, world, local):
     torch.cuda.synchronize()
 
     K = args.steps
+    # Phase-1 events bracket the reduction kernel on every EVERY-th step only:
+    # an event between two kernels stops the next one from being scheduled
+    # early (programmatic dependent launch), so most steps run without one.
+    EVERY = 8
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-           for _ in range(K)]
+           if i % EVERY == 0 else None for i in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     uuid = None
     try:
@@ -325,10 +341,10 @@ def run_gpu(args, wl, rank, world, local):
     clocks = sampler.summary(t_wall0, t_wall1)
 
     total_ms = start.elapsed_time(end)
-    reduce_ms = [a.elapsed_time(b) for (a, b) in evs]
-    t_max = max_over_ranks(total_ms / 1e3)
+    reduce_ms = [e[0].elapsed_time(e[1]) for e in evs if e is not None]
+    t_max = max_t(total_ms / 1e3)
     step_bytes = W * N * 2
-    value = world * step_bytes * K / t_max / 1e9
+    value = replica_value(world, step_bytes, K, t_max)
     ms_per_step = t_max * 1e3 / K
 
     # roofline of the dominant kernel (phase 1: tree reduce + norm partials)
@@ -354,7 +370,13 @@ def run_gpu(args, wl, rank, world, local):
     update_alg = N * (16 + 8 * min(1.0, kept_frac))    # in place: v,w r/w; kept: a, r, packed
     step_alg = k_alg + update_alg
 
-    # end to end: pinned host gradients -> device, step, result back to host
+    # End to end through the public API: every step moves all workers'
+    # gradients from pinned host memory to the GPU and reads the step's result
+    # (kept indices + threshold) back on the host.  Two ways of moving the
+    # gradients are timed: (a) one copy-engine copy into a device buffer
+    # followed by fc_step, (b) fc_step reading the pinned host buffer in
+    # place over the CPU-GPU link, so the reduction consumes the gradients
+    # as they arrive (the transfer and the reduction overlap).
     e2e = None
     if args.e2e_steps > 0:
         host = torch.empty(W * N, dtype=torch.float16, pin_memory=True)
@@ -365,46 +387,57 @@ def run_gpu(args, wl, rank, world, local):
                 hv[pos:pos + g.size] = g
                 pos += g.size
         stage = torch.empty(W * N, dtype=torch.float16, device=dev)
-        views, pos = [], 0
-        for w in range(W):
-            r = []
-            for n in wl.sizes:
-                r.append(stage[pos:pos + n])
-                pos += n
-            views.append(r)
-        etable = fc.PtrTable(views)
+
+        def views(buf):
+            out, p = [], 0
+            for w in range(W):
+                r = []
+                for n in wl.sizes:
+                    r.append(buf[p:p + n])
+                    p += n
+                out.append(r)
+            return out
+
         res_idx = torch.empty(eng.k, dtype=torch.int32, pin_memory=True)
         res_thr = torch.empty(1, dtype=torch.float32, pin_memory=True)
-        for _ in range(2):
-            with torch.cuda.stream(s):
-                stage.copy_(host, non_blocking=True)
-            eng.step(etable, s)
-            with torch.cuda.stream(s):
-                res_idx.copy_(eng.idx, non_blocking=True)
-                res_thr.copy_(eng.threshold, non_blocking=True)
-            s.synchronize()
-        barrier()
-        E = args.e2e_steps
-        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda.synchronize()
-        e0.record(s)
-        for _ in range(E):
-            with torch.cuda.stream(s):
-                stage.copy_(host, non_blocking=True)
-            eng.step(etable, s)
-            with torch.cuda.stream(s):
-                res_idx.copy_(eng.idx, non_blocking=True)
-                res_thr.copy_(eng.threshold, non_blocking=True)
-            s.synchronize()         # the host reads the step's result
-            _ = int(res_idx[0]), float(res_thr[0])
-        e1.record(s)
-        torch.cuda.synchronize()
-        et = max_over_ranks(e0.elapsed_time(e1) / 1e3)
-        e2e = {"value": round(world * step_bytes * E / et / 1e9, 3), "unit": UNIT,
+        variants = {}
+        for name, table, copy_in in (("copy_engine", fc.PtrTable(views(stage)), True),
+                                     ("zero_copy", fc.PtrTable(views(host)), False)):
+            def one_step():
+                if copy_in:
+                    with torch.cuda.stream(s):
+                        stage.copy_(host, non_blocking=True)
+                eng.step(table, s)
+                with torch.cuda.stream(s):
+                    res_idx.copy_(eng.idx, non_blocking=True)
+                    res_thr.copy_(eng.threshold, non_blocking=True)
+                s.synchronize()         # the host reads the step's result
+                return int(res_idx[0]), float(res_thr[0])
+
+            for _ in range(2):
+                one_step()
+            barrier()
+            E = args.e2e_steps
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            e0.record(s)
+            for _ in range(E):
+                one_step()
+            e1.record(s)
+            torch.cuda.synchronize()
+            et = max_t(e0.elapsed_time(e1) / 1e3)
+            variants[name] = {"value": round(replica_value(world, step_bytes, E, et), 3),
+                              "ms_per_step": round(et * 1e3 / E, 4), "steps": E}
+        best = max(variants, key=lambda k: variants[k]["value"])
+        e2e = {"value": variants[best]["value"], "unit": UNIT,
                "h2d_bytes_per_step": W * N * 2, "d2h_bytes_per_step": 4 * eng.k + 4,
-               "steps": E, "ms_per_step": round(et * 1e3 / E, 4),
-               "path": "one pinned-host -> device copy of all workers' gradients, fc_step, "
-                       "kept indices + threshold copied back and read on the host"}
+               "steps": variants[best]["steps"], "ms_per_step": variants[best]["ms_per_step"],
+               "path": {"copy_engine": "one pinned-host -> device copy of all workers' "
+                                       "gradients, then fc_step",
+                        "zero_copy": "fc_step reading the pinned host gradients in place "
+                                     "over the CPU-GPU link"}[best]
+                       + "; kept indices + threshold copied back and read on the host",
+               "variants": variants}
         del host, stage
 
     cpu = None
@@ -427,7 +460,8 @@ def run_gpu(args, wl, rank, world, local):
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
                          "traffic": traffic, "kernel": "k_reduce (fc_step_reduce)",
                          "algorithmic_bytes_per_launch": k_alg,
-                         "avg_launch_ms": round(k_ms, 5), "peak_source": peak_src + " hbm_gbs"},
+                         "avg_launch_ms": round(k_ms, 5), "peak_source": peak_src + " hbm_gbs",
+                         "timed_launches": len(reduce_ms)},
             "step_roofline": {"algorithmic_bytes_per_step": int(step_alg),
                               "achieved_gbs": round(step_alg / (ms_per_step / 1e3) / 1e9, 1),
                               "frac": round(step_alg / (ms_per_step / 1e3) / 1e9 / peak, 4),

@@ -221,10 +221,12 @@ fc_status fc_fuse_pack(const void *const *grads, int32_t W, int32_t L,
     return ok();
 }
 
-fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
-                         float loss_scale, const float *residual_in,
-                         float *out, void *stream)
+fc_status fc_reduce_ordered(const void *fused, int32_t W, int64_t N,
+                            float loss_scale, const float *residual_in,
+                            float *out, int32_t order, void *stream)
 {
+    if (order < FC_ORDER_TREE || order > FC_ORDER_RING)
+        return fail(FC_ERR_INVALID_ARG, "order = %d is not an FC_ORDER_* value", order);
     if (!fused) return fail(FC_ERR_INVALID_ARG, "fused is NULL");
     if (W < 1 || W > FC_MAX_TABLE_PTRS)
         return fail(FC_ERR_INVALID_ARG, "W = %d out of [1, %d]", W, FC_MAX_TABLE_PTRS);
@@ -245,16 +247,24 @@ fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
         const void *rows[256];
         for (int w = 0; w < W; ++w) rows[w] = (const __half *)fused + (int64_t)w * N;
         fill_table(tab, rows, W, 1, sizes);
-        e = launch_reduce(tab, G, u, residual_in, out, nullptr, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual_in, out, nullptr, (cudaStream_t)stream, order);
     } else {
         static thread_local TableL tab;
         static thread_local const void *rows[FC_MAX_TABLE_PTRS];
         for (int w = 0; w < W; ++w) rows[w] = (const __half *)fused + (int64_t)w * N;
         fill_table(tab, rows, W, 1, sizes);
-        e = launch_reduce(tab, G, u, residual_in, out, nullptr, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual_in, out, nullptr, (cudaStream_t)stream, order);
     }
-    if (e != cudaSuccess) return cuda_fail(e, "tree_reduce launch");
+    if (e != cudaSuccess) return cuda_fail(e, "reduce launch");
     return ok();
+}
+
+fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
+                         float loss_scale, const float *residual_in,
+                         float *out, void *stream)
+{
+    return fc_reduce_ordered(fused, W, N, loss_scale, residual_in, out,
+                             FC_ORDER_TREE, stream);
 }
 
 fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
@@ -286,13 +296,17 @@ static fc_status check_select_args(int64_t C, int64_t k, const int32_t *idx,
 fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
                           const float *a, int64_t N, int64_t chunk,
                           int32_t *idx, uint8_t *mask, float *packed,
+                          void *packed_fp16, float send_scale,
                           float *threshold, void *stream)
 {
     TRY(check_select_args(C, k, idx, mask, threshold));
     TRY(check_f32(norms, "norms", false));
-    if (packed) {
+    if (packed || packed_fp16) {
         TRY(check_f32(a, "a", false));
-        TRY(check_f32(packed, "packed", false));
+        TRY(check_f32(packed, "packed", true));
+        TRY(check_f32(packed_fp16, "packed_fp16", true));
+        if (!isfinite(send_scale))
+            return fail(FC_ERR_INVALID_ARG, "send_scale must be finite");
         if (chunk < 1 || N < 1 || ceil_div(N, chunk) != C)
             return fail(FC_ERR_INVALID_ARG, "N and chunk do not give C chunks");
     }
@@ -306,9 +320,9 @@ fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
     cudaError_t e = launch_select(G, nullptr, nullptr, const_cast<float *>(norms), k,
                                   idx, mask, nullptr, threshold, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "chunk_select launch");
-    if (packed) {
+    if (packed || packed_fp16) {
         e = launch_gather(a, N, chunk, ceil_div(chunk, FC_TILE), idx, k, packed,
-                          (cudaStream_t)stream);
+                          (__half *)packed_fp16, send_scale, (cudaStream_t)stream);
         if (e != cudaSuccess) return cuda_fail(e, "gather launch");
     }
     return ok();
@@ -344,7 +358,7 @@ fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
     TRY(bind_device(stream, a));
     const TileGeom G = geom(N, chunk);
     const int64_t tiles = ceil_div(N, chunk) * G.P;
-    cudaError_t e = launch_update(G, tiles, a, mask, nullptr, nullptr, lr,
+    cudaError_t e = launch_update(G, tiles, a, mask, nullptr, nullptr, nullptr, 1.f, lr,
                                   momentum, residual, velocity, weights,
                                   (__half *)weights_fp16, a == residual,
                                   (cudaStream_t)stream);
@@ -368,12 +382,15 @@ static fc_status check_ws(int64_t N, int64_t chunk, void *ws, size_t bytes)
     return FC_OK;
 }
 
-fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
-                         const int64_t *sizes, float loss_scale,
-                         int64_t chunk, const float *residual, float *a,
-                         void *workspace, size_t workspace_bytes,
-                         void *stream)
+fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
+                                 int32_t L, const int64_t *sizes,
+                                 float loss_scale, int64_t chunk,
+                                 const float *residual, float *a,
+                                 int32_t order, void *workspace,
+                                 size_t workspace_bytes, void *stream)
 {
+    if (order < FC_ORDER_TREE || order > FC_ORDER_RING)
+        return fail(FC_ERR_INVALID_ARG, "order = %d is not an FC_ORDER_* value", order);
     int64_t N = 0;
     TRY(check_sizes(L, sizes, &N));
     TRY(check_table(grads, W, L, sizes));
@@ -392,14 +409,25 @@ fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
     if (fits_small(W, L)) {
         TableS tab;
         fill_table(tab, grads, W, L, sizes);
-        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
     } else {
         static thread_local TableL tab;
         fill_table(tab, grads, W, L, sizes);
-        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream);
+        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
     }
     if (e != cudaSuccess) return cuda_fail(e, "step_reduce launch");
     return ok();
+}
+
+fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
+                         const int64_t *sizes, float loss_scale,
+                         int64_t chunk, const float *residual, float *a,
+                         void *workspace, size_t workspace_bytes,
+                         void *stream)
+{
+    return fc_step_reduce_ordered(grads, W, L, sizes, loss_scale, chunk,
+                                  residual, a, FC_ORDER_TREE, workspace,
+                                  workspace_bytes, stream);
 }
 
 fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
@@ -426,18 +454,22 @@ fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
 fc_status fc_step_update(const float *a, int64_t N, int64_t chunk, float lr,
                          float momentum, float *residual, float *velocity,
                          float *weights, void *weights_fp16,
-                         const uint8_t *mask, float *packed, void *workspace,
+                         const uint8_t *mask, float *packed,
+                         void *packed_fp16, float send_scale, void *workspace,
                          size_t workspace_bytes, void *stream)
 {
     TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
                           weights, weights_fp16));
     TRY(check_f32(packed, "packed", true));
+    TRY(check_f32(packed_fp16, "packed_fp16", true));
+    if (!isfinite(send_scale)) return fail(FC_ERR_INVALID_ARG, "send_scale must be finite");
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
     TRY(bind_device(stream, a));
     const TileGeom G = geom(N, chunk);
     const int64_t C = ceil_div(N, chunk);
     const int32_t *slot = (const int32_t *)((char *)workspace + ws_layout(N, chunk).slot);
-    cudaError_t e = launch_update(G, C * G.P, a, mask, slot, packed, lr,
+    cudaError_t e = launch_update(G, C * G.P, a, mask, slot, packed,
+                                  (__half *)packed_fp16, send_scale, lr,
                                   momentum, residual, velocity, weights,
                                   (__half *)weights_fp16, a == residual,
                                   (cudaStream_t)stream);
@@ -450,8 +482,9 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                   int64_t k, float lr, float momentum, float *residual,
                   float *a, float *velocity, float *weights,
                   void *weights_fp16, float *norms, int32_t *idx,
-                  uint8_t *mask, float *packed, float *threshold,
-                  void *workspace, size_t workspace_bytes, void *stream)
+                  uint8_t *mask, float *packed, void *packed_fp16,
+                  float send_scale, float *threshold, void *workspace,
+                  size_t workspace_bytes, void *stream)
 {
     int64_t N = 0;
     TRY(check_sizes(L, sizes, &N));
@@ -464,13 +497,15 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
     TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
                           weights, weights_fp16));
     TRY(check_f32(packed, "packed", true));
+    TRY(check_f32(packed_fp16, "packed_fp16", true));
+    if (!isfinite(send_scale)) return fail(FC_ERR_INVALID_ARG, "send_scale must be finite");
     TRY(fc_step_reduce(grads, W, L, sizes, loss_scale, chunk, residual, a,
                        workspace, workspace_bytes, stream));
     TRY(fc_step_select(N, chunk, k, norms, idx, mask, threshold, workspace,
                        workspace_bytes, stream));
     TRY(fc_step_update(a, N, chunk, lr, momentum, residual, velocity, weights,
-                       weights_fp16, mask, packed, workspace, workspace_bytes,
-                       stream));
+                       weights_fp16, mask, packed, packed_fp16, send_scale,
+                       workspace, workspace_bytes, stream));
     return ok();
 }
 

@@ -100,6 +100,24 @@ __device__ __forceinline__ int find_layer(const Tab &t, int64_t f)
     return lo;
 }
 
+// ---- programmatic dependent launch ---------------------------------------------
+//
+// The selection and update kernels are launched with programmatic stream
+// serialisation: the GPU may start them before the kernel ahead of them in
+// the stream has finished, and their first action is to wait (in hardware,
+// no polling) until that kernel has completed and its writes are visible.
+// The kernel ahead signals early that its dependents may be scheduled.
+
+__device__ __forceinline__ void wait_for_prior_grid()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+__device__ __forceinline__ void allow_dependent_launch()
+{
+    asm volatile("griddepcontrol.launch_dependents;" :::);
+}
+
 // ---- cache-hinted memory access ---------------------------------------------
 
 __device__ __forceinline__ uint64_t policy_evict_first()
@@ -228,6 +246,54 @@ __device__ __forceinline__ void tree_sum(int Wrt, Load &&load, float (&out)[V])
             }
         }
     }
+}
+
+// ---- other summation orders -------------------------------------------------------
+//
+// Left-to-right sum over the workers start, start+1, ..., start-1 (indices
+// modulo W): the parameter-server order (start = 0) and the ring
+// reduce-scatter order (start = the element's ring segment).  Loads are
+// issued eight at a time; the additions stay in order.
+
+__device__ __forceinline__ int ring_next(int w, int W) { return w + 1 == W ? 0 : w + 1; }
+
+template <int V, class Load>
+__device__ __forceinline__ void seq_sum(int W, int start, Load &&load,
+                                        float (&out)[V])
+{
+    int w = start;
+    load(w, out);
+    w = ring_next(w, W);
+    int t = 1;
+    for (; t + 8 <= W; t += 8) {
+        float x[8][V];
+        int ws[8];
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+            ws[u] = w;
+            w = ring_next(w, W);
+        }
+#pragma unroll
+        for (int u = 0; u < 8; ++u) load(ws[u], x[u]);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+#pragma unroll
+            for (int e = 0; e < V; ++e) out[e] = __fadd_rn(out[e], x[u][e]);
+    }
+    for (; t < W; ++t) {
+        float x[V];
+        load(w, x);
+#pragma unroll
+        for (int e = 0; e < V; ++e) out[e] = __fadd_rn(out[e], x[e]);
+        w = ring_next(w, W);
+    }
+}
+
+// Ring segment of fused index f: the s in [0, W) with
+// floor(s*N/W) <= f < floor((s+1)*N/W), i.e. floor(((f+1)*W - 1) / N).
+__device__ __forceinline__ int ring_segment(int64_t f, int64_t N, int W)
+{
+    return (int)(((f + 1) * (int64_t)W - 1) / N);
 }
 
 // ---- sums of squares ------------------------------------------------------------

@@ -15,11 +15,11 @@ bool fill_table(Tab &t, const void *const *grads, int32_t W, int32_t L,
                 const int64_t *sizes);
 
 // Phase-1 / fc_tree_reduce kernel launch.  With partials != NULL the unit
-// sums of squares go to partials [G.units].
+// sums of squares go to partials [G.units].  order: FC_ORDER_* of fc.h.
 template <class Tab>
 cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
                           const float *resid, float *out, float *partials,
-                          cudaStream_t s);
+                          cudaStream_t s, int order = 0);
 
 template <class Tab>
 cudaError_t launch_pack(const Tab &tab, int64_t N, __half *fused,
@@ -39,13 +39,13 @@ cudaError_t launch_select(const UnitGeom &G, const float *partials,
 
 cudaError_t launch_gather(const float *a, int64_t N, int64_t cs, int64_t P,
                           const int32_t *idx, int64_t k, float *packed,
-                          cudaStream_t s);
+                          __half *packed16, float send_scale, cudaStream_t s);
 
 cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           const uint8_t *mask, const int32_t *slot,
-                          float *packed, float lr, float mu, float *r,
-                          float *v, float *w, __half *w16, bool inplace,
-                          cudaStream_t s);
+                          float *packed, __half *packed16, float send_scale,
+                          float lr, float mu, float *r, float *v, float *w,
+                          __half *w16, bool inplace, cudaStream_t s);
 
 // Sets the calling thread's fc_last_error() message; returns st.
 fc_status set_error(fc_status st, const char *msg);
@@ -53,6 +53,27 @@ fc_status set_error(fc_status st, const char *msg);
 // Byte offset, inside the pipeline workspace for (N, chunk), of the 256-byte
 // word block that must be zero before a step.
 size_t step_ws_counter_offset(int64_t N, int64_t chunk);
+
+// Launches kernel<<<grid, block, smem, s>>>(args...) with programmatic
+// stream serialisation allowed (the kernel must begin with
+// wait_for_prior_grid()).
+template <typename... KArgs, typename... Args>
+cudaError_t launch_after_prior(void (*kernel)(KArgs...), unsigned grid,
+                               unsigned block, size_t smem, cudaStream_t s,
+                               Args... args)
+{
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
 
 // Blocks to launch for a grid-stride kernel: min(work, SMs * resident).
 int grid_for(const void *kernel, int block, size_t smem, int64_t work);

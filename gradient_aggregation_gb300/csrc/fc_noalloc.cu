@@ -56,6 +56,7 @@ fc_status fc_step_noalloc(const void *const *grads, int32_t W, int32_t L,
                           float *residual, float *a, float *velocity,
                           float *weights, void *weights_fp16, float *norms,
                           int32_t *idx, uint8_t *mask, float *packed,
+                          void *packed_fp16, float send_scale,
                           float *threshold, void *stream)
 {
     char msg[256];
@@ -100,7 +101,8 @@ fc_status fc_step_noalloc(const void *const *grads, int32_t W, int32_t L,
     }
     return fc_step(grads, W, L, sizes, loss_scale, chunk, k, lr, momentum,
                    residual, a, velocity, weights, weights_fp16, norms, idx,
-                   mask, packed, threshold, ws, need, stream);
+                   mask, packed, packed_fp16, send_scale, threshold, ws, need,
+                   stream);
 }
 
 }  // extern "C"

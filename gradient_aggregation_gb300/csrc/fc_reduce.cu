@@ -104,7 +104,9 @@ int grid_for(const void *kernel, int block, size_t smem, int64_t work)
 // `partials` given, the warp also writes the unit's sum of squares, which
 // the selection kernel turns into chunk norms.
 
-template <class Tab, int WT, int MAXH>
+// ORDER: 0 the binary tree, 1 parameter server (workers in index order),
+// 2 ring reduce-scatter (see fc_common.cuh).
+template <class Tab, int WT, int MAXH, int ORDER>
 __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0 && WT <= 16) ? 3 : 2))
     k_reduce(const __grid_constant__ Tab tab, const UnitGeom G, const float u,
              const float *resid, float *out, float *partials)
@@ -113,6 +115,7 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0
     const int W = WT > 0 ? WT : tab.W;
     const int L = tab.L;
     const int lane = threadIdx.x & 31;
+    allow_dependent_launch();  // the selection may be scheduled; it waits for us
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
 
     for (int64_t un = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
@@ -126,16 +129,22 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0
             float a[8];
             const bool full = (f0 >= lo) && (f0 + 8 <= hi);
             int l = find_layer(tab, f0 > lo ? f0 : lo);
-            if (full && f0 + 8 <= tab.off[l + 1] &&
+            // ring order: one start worker for the whole group, if the group
+            // lies in one ring segment
+            const int start = ORDER == 2 ? ring_segment(f0 > lo ? f0 : lo, G.N, W) : 0;
+            const bool one_start =
+                ORDER != 2 || ring_segment(f0 + 7 < hi ? f0 + 7 : hi - 1, G.N, W) == start;
+            if (full && one_start && f0 + 8 <= tab.off[l + 1] &&
                 ((tab.vec[l >> 5] >> (l & 31)) & 1u)) {
                 // vector path: 8 consecutive elements of one layer
                 const int64_t j = f0 - tab.off[l];
-                tree_sum<WT, MAXH, 8>(
-                    W,
-                    [&](int w, float(&x)[8]) {
-                        unpack8(ld_stream16(tab.ptr[w * L + l] + j, pol), x);
-                    },
-                    a);
+                auto ld8 = [&](int w, float(&x)[8]) {
+                    unpack8(ld_stream16(tab.ptr[w * L + l] + j, pol), x);
+                };
+                if constexpr (ORDER == 0)
+                    tree_sum<WT, MAXH, 8>(W, ld8, a);
+                else
+                    seq_sum<8>(W, start, ld8, a);
                 float r[8];
                 if (resid) {
                     const float4 r0 = __ldcs(reinterpret_cast<const float4 *>(resid + f0));
@@ -152,7 +161,8 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0
                 reinterpret_cast<float4 *>(out + f0)[1] = make_float4(a[4], a[5], a[6], a[7]);
             } else {
                 // element path: group clipped by the unit, crossing a layer
-                // boundary, or a layer whose workers are not 16-byte aligned
+                // or ring-segment boundary, or a layer whose workers are not
+                // 16-byte aligned
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
                     const int64_t f = f0 + e;
@@ -163,12 +173,13 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0
                     while (tab.off[l + 1] <= f) ++l;
                     const int64_t j = f - tab.off[l];
                     float s1[1];
-                    tree_sum<WT, MAXH, 1>(
-                        W,
-                        [&](int w, float(&x)[1]) {
-                            x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
-                        },
-                        s1);
+                    auto ld1 = [&](int w, float(&x)[1]) {
+                        x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
+                    };
+                    if constexpr (ORDER == 0)
+                        tree_sum<WT, MAXH, 1>(W, ld1, s1);
+                    else
+                        seq_sum<1>(W, ORDER == 2 ? ring_segment(f, G.N, W) : 0, ld1, s1);
                     float v = __fmul_rn(s1[0], u);
                     if (resid) v = __fadd_rn(v, __ldcs(resid + f));
                     out[f] = v;
@@ -184,12 +195,12 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0
     }
 }
 
-template <class Tab, int WT, int MAXH>
+template <class Tab, int WT, int MAXH, int ORDER = 0>
 static cudaError_t launch_reduce_w(const Tab &tab, const UnitGeom &G, float u,
                                    const float *resid, float *out,
                                    float *partials, cudaStream_t s)
 {
-    auto kern = k_reduce<Tab, WT, MAXH>;
+    auto kern = k_reduce<Tab, WT, MAXH, ORDER>;
     const int64_t blocks_needed = (G.units + FC_BLOCK / 32 - 1) / (FC_BLOCK / 32);
     const int grid = grid_for((const void *)kern, FC_BLOCK, 0, blocks_needed);
     kern<<<grid, FC_BLOCK, 0, s>>>(tab, G, u, resid, out, partials);
@@ -199,8 +210,10 @@ static cudaError_t launch_reduce_w(const Tab &tab, const UnitGeom &G, float u,
 template <class Tab>
 cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
                           const float *resid, float *out, float *partials,
-                          cudaStream_t s)
+                          cudaStream_t s, int order)
 {
+    if (order == 1) return launch_reduce_w<Tab, 0, 1, 1>(tab, G, u, resid, out, partials, s);
+    if (order == 2) return launch_reduce_w<Tab, 0, 1, 2>(tab, G, u, resid, out, partials, s);
     switch (tab.W) {
     case 1: return launch_reduce_w<Tab, 1, 1>(tab, G, u, resid, out, partials, s);
     case 2: return launch_reduce_w<Tab, 2, 2>(tab, G, u, resid, out, partials, s);
@@ -218,9 +231,9 @@ cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
 
 template cudaError_t launch_reduce<TableS>(const TableS &, const UnitGeom &,
                                            float, const float *, float *,
-                                           float *, cudaStream_t);
+                                           float *, cudaStream_t, int);
 template cudaError_t launch_reduce<TableL>(const TableL &, const UnitGeom &,
                                            float, const float *, float *,
-                                           float *, cudaStream_t);
+                                           float *, cudaStream_t, int);
 
 }  // namespace fc

@@ -17,7 +17,8 @@
 //    runs a 4-pass radix select (8 bits a pass) on their bit patterns, then
 //    one block scan in index order gives the tie-broken kept set, the
 //    ascending index list and each kept chunk's slot in the packed output;
-//  * gather: a grid-wide copy of the kept chunks into their slots.
+//  * gather: a grid-wide copy of the kept chunks into their slots (fp32
+//    and/or fp16 send buffers).
 #include "fc_internal.h"
 
 namespace fc {
@@ -162,6 +163,8 @@ __global__ void __launch_bounds__(SEL_THREADS)
     __shared__ uint32_t s_digit, s_rem, s_last;
     const int tid = threadIdx.x;
     const int64_t C = G.C;
+    wait_for_prior_grid();
+    allow_dependent_launch();
 
     if (partials) {
         const int lane = tid & 31, warp = tid >> 5;
@@ -197,10 +200,16 @@ __global__ void __launch_bounds__(SEL_THREADS)
         const int shift = 24 - 8 * pass;
         if (tid < 256) hist[tid] = 0;
         __syncthreads();
-        for (int64_t c = tid; c < C; c += SEL_THREADS) {
-            const uint32_t key = key_at(c);
-            if (pass == 0 || (key >> (shift + 8)) == prefix)
-                atomicAdd(&hist[(key >> shift) & 255u], 1u);
+        // Norms of similar size share their top bits, so many lanes hit the
+        // same bin: lanes with equal digits are counted once per warp.
+        for (int64_t base = tid & ~31; base < C; base += SEL_THREADS) {
+            const int64_t c = base + (tid & 31);
+            const uint32_t key = c < C ? key_at(c) : 0u;
+            const bool in = c < C && (pass == 0 || (key >> (shift + 8)) == prefix);
+            const uint32_t digit = in ? (key >> shift) & 255u : 256u;
+            const uint32_t peers = __match_any_sync(0xffffffffu, digit);
+            if (in && (tid & 31) == __ffs(peers) - 1)
+                atomicAdd(&hist[digit], (uint32_t)__popc(peers));
         }
         __syncthreads();
         if (tid < 32) {
@@ -281,9 +290,8 @@ cudaError_t launch_select(const UnitGeom &G, const float *partials,
         const int cap = grid_for((const void *)k_select, SEL_THREADS, 0, blocks);
         if (blocks > cap) blocks = cap;  // all blocks resident: no queueing
     }
-    k_select<<<(int)blocks, SEL_THREADS, 0, s>>>(G, partials, done, norms, k,
-                                                 idx, mask, slot, threshold);
-    return cudaGetLastError();
+    return launch_after_prior(k_select, (unsigned)blocks, SEL_THREADS, 0, s, G,
+                              partials, done, norms, k, idx, mask, slot, threshold);
 }
 
 // ---- packed copy of the kept chunks ----------------------------------------------
@@ -291,7 +299,8 @@ cudaError_t launch_select(const UnitGeom &G, const float *partials,
 __global__ void __launch_bounds__(FC_BLOCK)
     k_gather(const float *__restrict__ a, const int64_t N, const int64_t cs,
              const int64_t P, const int32_t *__restrict__ idx,
-             const int64_t tiles, float *__restrict__ packed)
+             const int64_t tiles, float *__restrict__ packed,
+             __half *__restrict__ packed16, const float send_scale)
 {
     const bool vec = (cs & 3) == 0;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
@@ -312,12 +321,24 @@ __global__ void __launch_bounds__(FC_BLOCK)
                     x.z = i + 2 < N ? a[i + 2] : 0.f;
                     x.w = i + 3 < N ? a[i + 3] : 0.f;
                 }
-                __stcs(reinterpret_cast<float4 *>(packed + dst + e), x);
+                if (packed) __stcs(reinterpret_cast<float4 *>(packed + dst + e), x);
+                if (packed16) {
+                    const __half2 s0 = __floats2half2_rn(__fmul_rn(x.x, send_scale),
+                                                         __fmul_rn(x.y, send_scale));
+                    const __half2 s1 = __floats2half2_rn(__fmul_rn(x.z, send_scale),
+                                                         __fmul_rn(x.w, send_scale));
+                    uint2 hv;
+                    hv.x = *reinterpret_cast<const uint32_t *>(&s0);
+                    hv.y = *reinterpret_cast<const uint32_t *>(&s1);
+                    __stcs(reinterpret_cast<uint2 *>(packed16 + dst + e), hv);
+                }
             }
         } else {
             for (int64_t e = e0 + threadIdx.x; e < e1; e += FC_BLOCK) {
                 const int64_t i = src + e;
-                packed[dst + e] = i < N ? __ldg(a + i) : 0.f;
+                const float x = i < N ? __ldg(a + i) : 0.f;
+                if (packed) packed[dst + e] = x;
+                if (packed16) packed16[dst + e] = __float2half_rn(__fmul_rn(x, send_scale));
             }
         }
     }
@@ -325,11 +346,12 @@ __global__ void __launch_bounds__(FC_BLOCK)
 
 cudaError_t launch_gather(const float *a, int64_t N, int64_t cs, int64_t P,
                           const int32_t *idx, int64_t k, float *packed,
-                          cudaStream_t s)
+                          __half *packed16, float send_scale, cudaStream_t s)
 {
     const int64_t tiles = k * P;
     const int grid = grid_for((const void *)k_gather, FC_BLOCK, 0, tiles);
-    k_gather<<<grid, FC_BLOCK, 0, s>>>(a, N, cs, P, idx, tiles, packed);
+    k_gather<<<grid, FC_BLOCK, 0, s>>>(a, N, cs, P, idx, tiles, packed, packed16,
+                                       send_scale);
     return cudaGetLastError();
 }
 

@@ -6,7 +6,9 @@
 // Caffe-compatible, appendix): v = momentum*v + lr*g, w = w - v.  Values of
 // chunks that were not sent (GradientFlow, arXiv 1902.06855, abstract:
 // coarse-grained sparse communication) are carried to the next step in an
-// fp32 residual instead of being dropped.
+// fp32 residual instead of being dropped.  The kept chunks are also written
+// to the send buffers: fp32, and/or fp16 (mixed-precision communication,
+// GradientFlow abstract) as binary16(a * send_scale).
 //
 // GB300 mapping: one streaming pass over the chunk-aligned tiles, so every
 // tile has a single kept/unkept decision (no per-element division); 16-byte
@@ -32,12 +34,14 @@ __device__ __forceinline__ void sgd1(float a, bool kept, float lr, float mu,
 __global__ void __launch_bounds__(FC_BLOCK)
     k_update(const TileGeom G, const int64_t tiles, const float *a,
              const uint8_t *__restrict__ mask, const int32_t *__restrict__ slot,
-             float *__restrict__ packed, const float lr, const float mu,
+             float *__restrict__ packed, __half *__restrict__ packed16,
+             const float send_scale, const float lr, const float mu,
              float *r, float *__restrict__ v, float *__restrict__ w,
              __half *__restrict__ w16, const int inplace)
 {
     const int64_t cs = G.cs;
     const bool pvec = (cs & 3) == 0;
+    wait_for_prior_grid();
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         int64_t lo, hi, c, hin;
         const bool any = tile_range(G, t, lo, hi, c, hin);
@@ -45,7 +49,8 @@ __global__ void __launch_bounds__(FC_BLOCK)
         const bool need_a = kept || !inplace;
         const bool write_r = kept || !inplace;
         // packed index of element i of a kept chunk: pbase + i
-        const int32_t sl = (packed != nullptr && kept) ? __ldg(slot + c) : -1;
+        const int32_t sl = ((packed != nullptr || packed16 != nullptr) && kept)
+                               ? __ldg(slot + c) : -1;
         const bool pk = sl >= 0;  // the slot map comes from the same selection
         const int64_t pbase = pk ? (int64_t)sl * cs - c * cs : 0;
         if (any) {
@@ -73,7 +78,7 @@ __global__ void __launch_bounds__(FC_BLOCK)
                         hv.y = *reinterpret_cast<uint32_t *>(&h1);
                         __stcs(reinterpret_cast<uint2 *>(w16 + i0), hv);
                     }
-                    if (pk) {
+                    if (pk && packed) {
                         if (pvec) {
                             __stcs(reinterpret_cast<float4 *>(packed + pbase + i0), av);
                         } else {
@@ -81,6 +86,23 @@ __global__ void __launch_bounds__(FC_BLOCK)
                             packed[pbase + i0 + 1] = av.y;
                             packed[pbase + i0 + 2] = av.z;
                             packed[pbase + i0 + 3] = av.w;
+                        }
+                    }
+                    if (pk && packed16) {
+                        const __half2 s0 = __floats2half2_rn(__fmul_rn(av.x, send_scale),
+                                                             __fmul_rn(av.y, send_scale));
+                        const __half2 s1 = __floats2half2_rn(__fmul_rn(av.z, send_scale),
+                                                             __fmul_rn(av.w, send_scale));
+                        if (pvec) {
+                            uint2 hv;
+                            hv.x = *reinterpret_cast<const uint32_t *>(&s0);
+                            hv.y = *reinterpret_cast<const uint32_t *>(&s1);
+                            __stcs(reinterpret_cast<uint2 *>(packed16 + pbase + i0), hv);
+                        } else {
+                            packed16[pbase + i0] = __low2half(s0);
+                            packed16[pbase + i0 + 1] = __high2half(s0);
+                            packed16[pbase + i0 + 2] = __low2half(s1);
+                            packed16[pbase + i0 + 3] = __high2half(s1);
                         }
                     }
                 } else {
@@ -94,7 +116,9 @@ __global__ void __launch_bounds__(FC_BLOCK)
                         w[i] = wi;
                         if (write_r) r[i] = ri;
                         if (w16) w16[i] = __float2half_rn(wi);
-                        if (pk) packed[pbase + i] = ai;
+                        if (pk && packed) packed[pbase + i] = ai;
+                        if (pk && packed16)
+                            packed16[pbase + i] = __float2half_rn(__fmul_rn(ai, send_scale));
                     }
                 }
             }
@@ -102,22 +126,24 @@ __global__ void __launch_bounds__(FC_BLOCK)
         // zero the packed slot beyond N (short last chunk)
         if (pk && hin > hi) {
             const int64_t p0 = lo > G.N ? lo : G.N;
-            for (int64_t i = p0 + threadIdx.x; i < hin; i += FC_BLOCK)
-                packed[pbase + i] = 0.f;
+            for (int64_t i = p0 + threadIdx.x; i < hin; i += FC_BLOCK) {
+                if (packed) packed[pbase + i] = 0.f;
+                if (packed16) packed16[pbase + i] = __float2half_rn(0.f);
+            }
         }
     }
 }
 
 cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           const uint8_t *mask, const int32_t *slot,
-                          float *packed, float lr, float mu, float *r,
-                          float *v, float *w, __half *w16, bool inplace,
-                          cudaStream_t s)
+                          float *packed, __half *packed16, float send_scale,
+                          float lr, float mu, float *r, float *v, float *w,
+                          __half *w16, bool inplace, cudaStream_t s)
 {
     const int grid = grid_for((const void *)k_update, FC_BLOCK, 0, tiles);
-    k_update<<<grid, FC_BLOCK, 0, s>>>(G, tiles, a, mask, slot, packed, lr, mu,
-                                       r, v, w, w16, inplace ? 1 : 0);
-    return cudaGetLastError();
+    return launch_after_prior(k_update, (unsigned)grid, FC_BLOCK, 0, s, G, tiles,
+                              a, mask, slot, packed, packed16, send_scale, lr,
+                              mu, r, v, w, w16, inplace ? 1 : 0);
 }
 
 }  // namespace fc

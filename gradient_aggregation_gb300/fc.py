@@ -28,6 +28,7 @@ FC_ERR_LIMIT = -5
 FC_MAX_TABLE_PTRS = 3072
 FC_MAX_TABLE_LAYERS = 512
 FC_NOALLOC_WORKSPACE_BYTES = 4 << 20
+FC_ORDER_TREE, FC_ORDER_SEQUENTIAL, FC_ORDER_RING = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -42,17 +43,22 @@ _SIGS = {
     "fc_layout": (ctypes.c_int, [_I32, _P, _P, _P]),
     "fc_fuse_pack": (ctypes.c_int, [_P, _I32, _I32, _P, _P, _P, _P]),
     "fc_tree_reduce": (ctypes.c_int, [_P, _I32, _I64, _F32, _P, _P, _P]),
+    "fc_reduce_ordered": (ctypes.c_int, [_P, _I32, _I64, _F32, _P, _P, _I32, _P]),
+    "fc_step_reduce_ordered": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _I32,
+                                              _P, _SZ, _P]),
     "fc_chunk_norms": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
-    "fc_chunk_select": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _P, _P]),
+    "fc_chunk_select": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _P, _F32,
+                                       _P, _P]),
     "fc_residual_sgd_update": (ctypes.c_int, [_P, _P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P]),
     "fc_step_workspace_size": (_SZ, [_I64, _I64]),
     "fc_step_reduce": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _P, _SZ, _P]),
     "fc_step_select": (ctypes.c_int, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
-    "fc_step_update": (ctypes.c_int, [_P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+    "fc_step_update": (ctypes.c_int, [_P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P, _P, _P,
+                                      _F32, _P, _SZ, _P]),
     "fc_step": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _I64, _F32, _F32, _P, _P, _P,
-                               _P, _P, _P, _P, _P, _P, _P, _P, _SZ, _P]),
+                               _P, _P, _P, _P, _P, _P, _P, _F32, _P, _P, _SZ, _P]),
     "fc_step_noalloc": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _I64, _F32, _F32, _P,
-                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _P]),
+                                       _P, _P, _P, _P, _P, _P, _P, _P, _P, _F32, _P, _P]),
 }
 
 
@@ -180,6 +186,13 @@ def fc_tree_reduce(fused: torch.Tensor, W: int, N: int, loss_scale: float,
                                 _p(residual_in), _p(out), _s(stream)))
 
 
+def fc_reduce_ordered(fused: torch.Tensor, W: int, N: int, loss_scale: float,
+                      residual_in: Optional[torch.Tensor], out: torch.Tensor, order: int,
+                      stream=None) -> None:
+    _check(lib().fc_reduce_ordered(_p(fused), int(W), int(N), float(loss_scale),
+                                   _p(residual_in), _p(out), int(order), _s(stream)))
+
+
 def fc_chunk_norms(a: torch.Tensor, N: int, chunk: int, norms: torch.Tensor,
                    stream=None) -> None:
     _check(lib().fc_chunk_norms(_p(a), int(N), int(chunk), _p(norms), _s(stream)))
@@ -188,9 +201,11 @@ def fc_chunk_norms(a: torch.Tensor, N: int, chunk: int, norms: torch.Tensor,
 def fc_chunk_select(norms: torch.Tensor, C: int, k: int, a: Optional[torch.Tensor],
                     N: int, chunk: int, idx: torch.Tensor, mask: torch.Tensor,
                     packed: Optional[torch.Tensor], threshold: torch.Tensor,
+                    packed_fp16: Optional[torch.Tensor] = None, send_scale: float = 1.0,
                     stream=None) -> None:
     _check(lib().fc_chunk_select(_p(norms), int(C), int(k), _p(a), int(N), int(chunk),
-                                 _p(idx), _p(mask), _p(packed), _p(threshold), _s(stream)))
+                                 _p(idx), _p(mask), _p(packed), _p(packed_fp16),
+                                 float(send_scale), _p(threshold), _s(stream)))
 
 
 def fc_residual_sgd_update(a: torch.Tensor, mask: torch.Tensor, N: int, chunk: int,
@@ -214,6 +229,15 @@ def fc_step_reduce(grads, loss_scale: float, chunk: int,
                                 _s(stream)))
 
 
+def fc_step_reduce_ordered(grads, loss_scale: float, chunk: int,
+                           residual: Optional[torch.Tensor], a: torch.Tensor, order: int,
+                           workspace: torch.Tensor, stream=None) -> None:
+    t = _table(grads)
+    _check(lib().fc_step_reduce_ordered(t.ptrs, t.W, t.L, t.sizes_c, float(loss_scale),
+                                        int(chunk), _p(residual), _p(a), int(order),
+                                        _p(workspace), workspace.numel(), _s(stream)))
+
+
 def fc_step_select(N: int, chunk: int, k: int, norms: torch.Tensor, idx: torch.Tensor,
                    mask: torch.Tensor, threshold: torch.Tensor, workspace: torch.Tensor,
                    stream=None) -> None:
@@ -225,11 +249,12 @@ def fc_step_update(a: torch.Tensor, N: int, chunk: int, lr: float, momentum: flo
                    residual: torch.Tensor, velocity: torch.Tensor, weights: torch.Tensor,
                    weights_fp16: Optional[torch.Tensor], mask: torch.Tensor,
                    packed: Optional[torch.Tensor], workspace: torch.Tensor,
+                   packed_fp16: Optional[torch.Tensor] = None, send_scale: float = 1.0,
                    stream=None) -> None:
     _check(lib().fc_step_update(_p(a), int(N), int(chunk), float(lr), float(momentum),
                                 _p(residual), _p(velocity), _p(weights), _p(weights_fp16),
-                                _p(mask), _p(packed), _p(workspace), workspace.numel(),
-                                _s(stream)))
+                                _p(mask), _p(packed), _p(packed_fp16), float(send_scale),
+                                _p(workspace), workspace.numel(), _s(stream)))
 
 
 def fc_step(grads, loss_scale: float, chunk: int, k: int, lr: float, momentum: float,
@@ -237,13 +262,14 @@ def fc_step(grads, loss_scale: float, chunk: int, k: int, lr: float, momentum: f
             weights: torch.Tensor, weights_fp16: Optional[torch.Tensor],
             norms: torch.Tensor, idx: torch.Tensor, mask: torch.Tensor,
             packed: Optional[torch.Tensor], threshold: torch.Tensor,
-            workspace: torch.Tensor, stream=None) -> None:
+            workspace: torch.Tensor, stream=None,
+            packed_fp16: Optional[torch.Tensor] = None, send_scale: float = 1.0) -> None:
     t = _table(grads)
     _check(lib().fc_step(t.ptrs, t.W, t.L, t.sizes_c, float(loss_scale), int(chunk), int(k),
                          float(lr), float(momentum), _p(residual), _p(a), _p(velocity),
                          _p(weights), _p(weights_fp16), _p(norms), _p(idx), _p(mask),
-                         _p(packed), _p(threshold), _p(workspace), workspace.numel(),
-                         _s(stream)))
+                         _p(packed), _p(packed_fp16), float(send_scale), _p(threshold),
+                         _p(workspace), workspace.numel(), _s(stream)))
 
 
 def fc_step_noalloc(grads, loss_scale: float, chunk: int, k: int, lr: float,
@@ -251,7 +277,9 @@ def fc_step_noalloc(grads, loss_scale: float, chunk: int, k: int, lr: float,
                     velocity: torch.Tensor, weights: torch.Tensor,
                     weights_fp16: Optional[torch.Tensor], norms: torch.Tensor,
                     idx: torch.Tensor, mask: torch.Tensor, packed: Optional[torch.Tensor],
-                    threshold: torch.Tensor, stream=None) -> None:
+                    threshold: torch.Tensor, stream=None,
+                    packed_fp16: Optional[torch.Tensor] = None,
+                    send_scale: float = 1.0) -> None:
     """fc_step with the library's built-in scratch array instead of a
     caller workspace, for callers that cannot allocate device memory when
     they step (see include/fc.h)."""
@@ -259,7 +287,8 @@ def fc_step_noalloc(grads, loss_scale: float, chunk: int, k: int, lr: float,
     _check(lib().fc_step_noalloc(t.ptrs, t.W, t.L, t.sizes_c, float(loss_scale), int(chunk),
                                  int(k), float(lr), float(momentum), _p(residual), _p(a),
                                  _p(velocity), _p(weights), _p(weights_fp16), _p(norms),
-                                 _p(idx), _p(mask), _p(packed), _p(threshold), _s(stream)))
+                                 _p(idx), _p(mask), _p(packed), _p(packed_fp16),
+                                 float(send_scale), _p(threshold), _s(stream)))
 
 
 # ---- engine: device buffers for repeated steps ---------------------------------------
@@ -277,7 +306,8 @@ class Engine:
     def __init__(self, sizes: Sequence[int], W: int, chunk: int, keep_num: int,
                  keep_den: int, loss_scale: float, lr: float, momentum: float,
                  weights: torch.Tensor, want_fp16: bool = False,
-                 want_packed: bool = True, keep_a: bool = False):
+                 want_packed: bool = True, keep_a: bool = False,
+                 want_packed_fp16: bool = False, send_scale: float = 1.0):
         dev = weights.device
         self.sizes = [int(s) for s in sizes]
         self.W = int(W)
@@ -297,6 +327,9 @@ class Engine:
         self.mask = torch.empty(self.C, dtype=torch.uint8, device=dev)
         self.packed = (torch.empty(self.k * self.chunk, dtype=torch.float32, device=dev)
                        if want_packed else None)
+        self.packed_fp16 = (torch.empty(self.k * self.chunk, dtype=torch.float16, device=dev)
+                            if want_packed_fp16 else None)
+        self.send_scale = float(send_scale)
         self.threshold = torch.empty(1, dtype=torch.float32, device=dev)
         # zero-filled once; the pipeline keeps its counters at zero
         self.workspace = torch.zeros(fc_step_workspace_size(self.N, self.chunk),
@@ -306,7 +339,7 @@ class Engine:
         fc_step(grads, self.loss_scale, self.chunk, self.k, self.lr, self.momentum,
                 self.residual, self.a, self.velocity, self.weights, self.weights_fp16,
                 self.norms, self.idx, self.mask, self.packed, self.threshold,
-                self.workspace, stream)
+                self.workspace, stream, self.packed_fp16, self.send_scale)
 
     def phases(self, grads, stream=None):
         """The three phases as separate calls (for per-phase timing)."""
@@ -317,7 +350,8 @@ class Engine:
         yield lambda: fc_step_update(self.a, self.N, self.chunk, self.lr, self.momentum,
                                      self.residual, self.velocity, self.weights,
                                      self.weights_fp16, self.mask, self.packed,
-                                     self.workspace, stream)
+                                     self.workspace, self.packed_fp16, self.send_scale,
+                                     stream)
 
     def state_dict(self) -> dict:
         return {"residual": self.residual.clone(), "velocity": self.velocity.clone(),

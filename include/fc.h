@@ -141,6 +141,28 @@ FC_API fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
                          float loss_scale, const float *residual_in,
                          float *out, void *stream);
 
+/* Summation orders over the workers.  The engine's method is the binary
+ * tree; the other two are the aggregation schemes the pages set the tree
+ * against, with the same operations in another order (results differ from
+ * the tree's by fp32 rounding only):
+ *  FC_ORDER_TREE        FireCaffe §6 reduction tree (as above);
+ *  FC_ORDER_SEQUENTIAL  parameter server (FireCaffe §6: one node receives
+ *                       and sums every worker's gradient): ((x0+x1)+x2)+...;
+ *  FC_ORDER_RING        ring reduce-scatter (GradientFlow abstract, ring-
+ *                       based allreduce): the fused vector is cut into W
+ *                       segments [floor(s*N/W), floor((s+1)*N/W)); the sum of
+ *                       segment s starts at worker s and goes round the ring:
+ *                       ((x_s + x_{s+1}) + ...) + x_{s-1}, indices mod W. */
+#define FC_ORDER_TREE 0
+#define FC_ORDER_SEQUENTIAL 1
+#define FC_ORDER_RING 2
+
+/* fc_tree_reduce with a selectable summation order (FC_ORDER_*); the
+ * FC_ORDER_TREE result is bit-identical to fc_tree_reduce. */
+FC_API fc_status fc_reduce_ordered(const void *fused, int32_t W, int64_t N,
+                                   float loss_scale, const float *residual_in,
+                                   float *out, int32_t order, void *stream);
+
 /* ---- a3: chunk norms ---------------------------------------------------------- */
 
 /* norms[c] = sqrt(sum_{i in chunk c} a[i]^2), c < C = fc_num_chunks(N, chunk).
@@ -159,18 +181,23 @@ FC_API fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
  * order, found by a radix select on the norms' bit patterns.
  *  norms      device fp32 [C], finite and >= 0.
  *  a, N, chunk  the reduced gradient the norms were taken over (a device fp32
- *             [N]); only read when packed != NULL.
+ *             [N]); only read when a send buffer is asked for.
  *  idx        device int32 [k] output: kept chunk indices, ascending.
  *  mask       device uint8 [C] output: 1 = kept.
- *  packed     device fp32 [k*chunk] output or NULL: kept chunks' values of a
- *             in idx order, one `chunk`-float slot each, the short last chunk
- *             zero-padded.
+ *  packed     device fp32 [k*chunk] output or NULL: the send buffer, kept
+ *             chunks' values of a in idx order, one `chunk`-float slot each,
+ *             the short last chunk zero-padded.
+ *  packed_fp16  device fp16 [k*chunk] output or NULL: the same send buffer
+ *             in fp16 (GradientFlow abstract: mixed-precision communication),
+ *             fp16_rne(value * send_scale); send_scale (finite) typically
+ *             puts the values back in fp16 range, e.g. the loss scale.
  *  threshold  device fp32 [1] output: the norm of the k-th kept chunk.
  * 1 <= k <= C. */
 FC_API fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
-                          const float *a, int64_t N, int64_t chunk,
-                          int32_t *idx, uint8_t *mask, float *packed,
-                          float *threshold, void *stream);
+                                 const float *a, int64_t N, int64_t chunk,
+                                 int32_t *idx, uint8_t *mask, float *packed,
+                                 void *packed_fp16, float send_scale,
+                                 float *threshold, void *stream);
 
 /* ---- a5: residual fold and momentum SGD ---------------------------------------- */
 
@@ -213,6 +240,15 @@ FC_API fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,
                                 void *workspace, size_t workspace_bytes,
                                 void *stream);
 
+/* fc_step_reduce with a selectable summation order (FC_ORDER_*); the
+ * FC_ORDER_TREE call is fc_step_reduce. */
+FC_API fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
+                                        int32_t L, const int64_t *sizes,
+                                        float loss_scale, int64_t chunk,
+                                        const float *residual, float *a,
+                                        int32_t order, void *workspace,
+                                        size_t workspace_bytes, void *stream);
+
 /* Phase 2: finishes the chunk norms from phase 1's unit sums (norms [C],
  * device output, bitwise the same as fc_chunk_norms on a) and selects the
  * top k chunks exactly as fc_chunk_select does (idx [k], mask [C],
@@ -224,25 +260,28 @@ FC_API fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k,
                                 size_t workspace_bytes, void *stream);
 
 /* Phase 3: the a5 update of fc_residual_sgd_update, which also writes the
- * kept chunks into `packed` (device fp32 [k*chunk] or NULL, laid out as in
- * fc_chunk_select).  `mask` must be the one phase 2 wrote.  When
- * a == residual (in place), unkept elements already hold their new residual
- * and are neither read nor rewritten. */
+ * kept chunks into the send buffers `packed` (device fp32 [k*chunk] or NULL)
+ * and `packed_fp16` (device fp16 [k*chunk] or NULL, values times
+ * send_scale), laid out as in fc_chunk_select.  `mask` must be the one
+ * phase 2 wrote.  When a == residual (in place), unkept elements already
+ * hold their new residual and are neither read nor rewritten. */
 FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk,
                                 float lr, float momentum, float *residual,
                                 float *velocity, float *weights,
                                 void *weights_fp16, const uint8_t *mask,
-                                float *packed, void *workspace,
+                                float *packed, void *packed_fp16,
+                                float send_scale, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
 /* Phases 1-3 in one call on one stream (three kernel launches). */
 FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
-                  const int64_t *sizes, float loss_scale, int64_t chunk,
-                  int64_t k, float lr, float momentum, float *residual,
-                  float *a, float *velocity, float *weights,
-                  void *weights_fp16, float *norms, int32_t *idx,
-                  uint8_t *mask, float *packed, float *threshold,
-                  void *workspace, size_t workspace_bytes, void *stream);
+                         const int64_t *sizes, float loss_scale, int64_t chunk,
+                         int64_t k, float lr, float momentum, float *residual,
+                         float *a, float *velocity, float *weights,
+                         void *weights_fp16, float *norms, int32_t *idx,
+                         uint8_t *mask, float *packed, void *packed_fp16,
+                         float send_scale, float *threshold, void *workspace,
+                         size_t workspace_bytes, void *stream);
 
 /* ---- the pipeline without a caller workspace ---------------------------------- */
 
@@ -277,6 +316,7 @@ FC_API fc_status fc_step_noalloc(const void *const *grads, int32_t W,
                                  float *a, float *velocity, float *weights,
                                  void *weights_fp16, float *norms,
                                  int32_t *idx, uint8_t *mask, float *packed,
+                                 void *packed_fp16, float send_scale,
                                  float *threshold, void *stream);
 
 #ifdef __cplusplus

@@ -68,6 +68,10 @@ def _load():
             "orc_keep_count": (i64, [i64, i64, i64]),
             "orc_chunk_select": (None, [P, i64, i64, P, i64, i64, P, P, P, P]),
             "orc_residual_sgd_update": (None, [P, P, i64, i64, f32, f32, P, P, P, P]),
+            "orc_pack_fp16": (None, [P, i64, f32, P]),
+            "orc_sequential_sum": (f32, [P, i32]),
+            "orc_ring_segment": (i32, [i64, i64, i32]),
+            "orc_reduce_ordered": (None, [i32, i64, P, f32, P, P, i32]),
         }
         for name, (res, args) in sig.items():
             fn = getattr(lib, name)
@@ -143,6 +147,32 @@ def tree_reduce(fused: np.ndarray, loss_scale: float,
     return out
 
 
+ORDER_TREE, ORDER_SEQUENTIAL, ORDER_RING = 0, 1, 2
+
+
+def sequential_sum(x: Sequence[float]) -> np.float32:
+    """Left-to-right fp32 sum (parameter-server order, FireCaffe §6)."""
+    a = _c(x, np.float32).copy()
+    return np.float32(_load().orc_sequential_sum(_ptr(a), len(a)))
+
+
+def ring_segment(i: int, N: int, W: int) -> int:
+    return int(_load().orc_ring_segment(int(i), int(N), int(W)))
+
+
+def reduce_ordered(fused: np.ndarray, loss_scale: float,
+                   residual: Optional[np.ndarray] = None, order: int = 0) -> np.ndarray:
+    """a2 with a selectable summation order: 0 tree, 1 parameter server
+    (sequential), 2 ring reduce-scatter (GradientFlow abstract)."""
+    f = _c(fused, np.float16)
+    W, N = f.shape
+    r = None if residual is None else _c(residual, np.float32)
+    out = np.empty(N, dtype=np.float32)
+    _load().orc_reduce_ordered(W, N, _ptr(f), float(loss_scale), _ptr(r), _ptr(out),
+                               int(order))
+    return out
+
+
 # ---- a3: norms --------------------------------------------------------------
 
 def num_chunks(N: int, chunk: int) -> int:
@@ -181,6 +211,15 @@ def chunk_select(norms: np.ndarray, k: int, a: Optional[np.ndarray] = None,
     _load().orc_chunk_select(_ptr(n), C, int(k), _ptr(av), int(N), int(chunk),
                              _ptr(idx), _ptr(mask), _ptr(packed), _ptr(thr))
     return idx, mask, packed, np.float32(thr[0])
+
+
+def pack_fp16(packed: np.ndarray, send_scale: float = 1.0) -> np.ndarray:
+    """fp16 send buffer of the packed kept chunks (GradientFlow abstract:
+    mixed precision): binary16(packed * send_scale), as uint16 bits."""
+    p = _c(packed, np.float32)
+    out = np.empty(p.size, dtype=np.uint16)
+    _load().orc_pack_fp16(_ptr(p), p.size, float(send_scale), _ptr(out))
+    return out
 
 
 # ---- a5: update -------------------------------------------------------------

@@ -167,6 +167,63 @@ void orc_tree_reduce(int32_t W, int64_t N, const uint16_t *fused,
     free(x);
 }
 
+/* ---- a2 with other summation orders ------------------------------------ */
+/* The pages contrast the tree with a parameter server (FireCaffe §6: one
+ * node receives every worker's gradient and sums them) and name ring-based
+ * allreduce (GradientFlow abstract).  Their fp32 results differ from the
+ * tree's by rounding only; the engine offers them as selectable orders.
+ *   order 0: the binary tree above;
+ *   order 1: parameter server, workers added one after another in index
+ *            order: ((x0 + x1) + x2) + ... ;
+ *   order 2: ring reduce-scatter: the fused vector is cut into W segments,
+ *            segment s = [floor(s*N/W), floor((s+1)*N/W)); the partial sum of
+ *            segment s starts at worker s and travels around the ring, each
+ *            worker adding its own value: ((x_s + x_{s+1}) + ...) + x_{s-1},
+ *            indices modulo W. */
+
+/* x[0] + x[1] + ... + x[m-1], added left to right. */
+float orc_sequential_sum(const float *x, int32_t m)
+{
+    float acc = x[0];
+    for (int32_t j = 1; j < m; ++j) acc = acc + x[j];
+    return acc;
+}
+
+/* Segment of fused index i: the s with floor(s*N/W) <= i < floor((s+1)*N/W). */
+int32_t orc_ring_segment(int64_t i, int64_t N, int32_t W)
+{
+    int32_t s = 0;
+    while (s + 1 < W && ((int64_t)(s + 1) * N) / W <= i) ++s;
+    return s;
+}
+
+void orc_reduce_ordered(int32_t W, int64_t N, const uint16_t *fused,
+                        float loss_scale, const float *residual, float *out,
+                        int32_t order)
+{
+    if (order == 0) {
+        orc_tree_reduce(W, N, fused, loss_scale, residual, out);
+        return;
+    }
+    float *x = (float *)malloc(sizeof(float) * (size_t)W);
+    float inv = orc_unscale_factor(loss_scale, W);
+    int32_t seg = 0;
+    for (int64_t i = 0; i < N; ++i) {
+        int32_t start = 0;
+        if (order == 2) {
+            while (seg + 1 < W && ((int64_t)(seg + 1) * N) / W <= i) ++seg;
+            start = seg;
+        }
+        for (int32_t t = 0; t < W; ++t)
+            x[t] = orc_half_to_float(fused[(int64_t)((start + t) % W) * N + i]);
+        float s = orc_sequential_sum(x, W);
+        float a = s * inv;
+        if (residual) a = a + residual[i];
+        out[i] = a;
+    }
+    free(x);
+}
+
 /* ---- a3: chunk L2 norms -------------------------------------------------- */
 
 int64_t orc_num_chunks(int64_t N, int64_t chunk)
@@ -245,6 +302,17 @@ void orc_chunk_select(const float *norms, int64_t C, int64_t k,
         ++q;
     }
     free(order);
+}
+
+/* fp16 send buffer of the kept chunks (mixed-precision communication,
+ * GradientFlow abstract): out[j] = binary16(packed[j] * send_scale), each a
+ * binary32 product rounded to nearest even, then rounded to binary16 (ties
+ * to even, overflow to infinity).  The zero padding stays +0. */
+void orc_pack_fp16(const float *packed, int64_t n, float send_scale,
+                   uint16_t *out)
+{
+    for (int64_t j = 0; j < n; ++j)
+        out[j] = orc_float_to_half(packed[j] * send_scale);
 }
 
 /* ---- a5: residual fold and momentum SGD ----------------------------------- */

@@ -34,7 +34,8 @@ class GpuRun:
     def __init__(self, wl: workload.Workload, path: str = "pipeline",
                  inplace: bool = False, want_w16: bool = True,
                  want_packed: bool = True, device: str = "cuda",
-                 weights: np.ndarray = None):
+                 weights: np.ndarray = None, want_packed16: bool = True,
+                 send_scale: float = None):
         self.wl, self.path, self.inplace = wl, path, inplace
         N, W = wl.N, wl.W
         self.N = N
@@ -51,6 +52,9 @@ class GpuRun:
         self.mask = torch.empty(self.C, dtype=torch.uint8, device=device)
         self.packed = (torch.empty(self.k * wl.chunk, dtype=torch.float32, device=device)
                        if want_packed else None)
+        self.packed16 = (torch.empty(self.k * wl.chunk, dtype=torch.float16, device=device)
+                         if want_packed16 else None)
+        self.send_scale = float(wl.loss_scale if send_scale is None else send_scale)
         self.threshold = torch.empty(1, dtype=torch.float32, device=device)
         self.ws = torch.zeros(fc.fc_step_workspace_size(N, wl.chunk), dtype=torch.uint8,
                               device=device)
@@ -64,14 +68,15 @@ class GpuRun:
             fc.fc_step(grads_dev, wl.loss_scale, wl.chunk, self.k, wl.lr, wl.momentum,
                        self.residual, self.a, self.velocity, self.weights, self.w16,
                        self.norms, self.idx, self.mask, self.packed, self.threshold,
-                       self.ws, stream)
+                       self.ws, stream, self.packed16, self.send_scale)
         else:
             self.offsets = fc.fc_fuse_pack(grads_dev, self.fused, stream)
             fc.fc_tree_reduce(self.fused, wl.W, self.N, wl.loss_scale, self.residual,
                               self.a, stream)
             fc.fc_chunk_norms(self.a, self.N, wl.chunk, self.norms, stream)
             fc.fc_chunk_select(self.norms, self.C, self.k, self.a, self.N, wl.chunk,
-                               self.idx, self.mask, self.packed, self.threshold, stream)
+                               self.idx, self.mask, self.packed, self.threshold,
+                               self.packed16, self.send_scale, stream)
             fc.fc_residual_sgd_update(self.a, self.mask, self.N, wl.chunk, wl.lr,
                                       wl.momentum, self.residual, self.velocity,
                                       self.weights, self.w16, stream)
@@ -88,6 +93,9 @@ class GpuRun:
             out["a"] = self.a.cpu().numpy()
         if self.packed is not None:
             out["packed"] = self.packed.cpu().numpy()
+        if self.packed16 is not None:
+            out["packed16"] = self.packed16.cpu().numpy().view(np.uint16)
+            out["send_scale"] = self.send_scale
         if self.w16 is not None:
             out["w16"] = self.w16.cpu().numpy().view(np.uint16)
         if self.fused is not None:
@@ -147,6 +155,11 @@ def oracle_step(grads_np, st: oracle.State, wl: workload.Workload, gpu: dict,
         if same_mask:
             assert bits_equal(exp, packed)
         assert bits_equal(gpu["packed"], exp), "packed differs"
+        if "packed16" in gpu:
+            exp16 = oracle.pack_fp16(exp, gpu["send_scale"])
+            assert_close("packed16", gpu["packed16"].view(np.float16).astype(np.float32),
+                         exp16.view(np.float16).astype(np.float32), RTOL_F16)
+            assert bits_equal(gpu["packed16"], exp16), "fp16 send buffer differs"
     # the update, following the GPU's kept set (identical outside the band)
     w16 = oracle.residual_sgd_update(a, gmask, wl.chunk, wl.lr, wl.momentum, st.residual,
                                      st.velocity, st.weights, want_w16="w16" in gpu)

@@ -96,10 +96,12 @@ def test_argument_errors_return_before_any_device_work(fc_lib):
     assert L.fc_chunk_norms(fake, 10, 0, fake, None) == fc.FC_ERR_INVALID_ARG
     assert L.fc_chunk_norms(fake + 8, 10, 4, fake, None) == fc.FC_ERR_ALIGNMENT
     # select
-    assert L.fc_chunk_select(fake, 4, 5, None, 0, 0, fake, fake, None, fake, None) == fc.FC_ERR_INVALID_ARG
-    assert L.fc_chunk_select(fake, 4, 0, None, 0, 0, fake, fake, None, fake, None) == fc.FC_ERR_INVALID_ARG
-    assert L.fc_chunk_select(fake, 4, 2, None, 0, 0, None, fake, None, fake, None) == fc.FC_ERR_INVALID_ARG
-    assert L.fc_chunk_select(fake, 4, 2, fake, 100, 10, fake, fake, fake, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 5, None, 0, 0, fake, fake, None, None, 1.0, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 0, None, 0, 0, fake, fake, None, None, 1.0, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 2, None, 0, 0, None, fake, None, None, 1.0, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 2, fake, 100, 10, fake, fake, fake, None, 1.0, fake, None) == fc.FC_ERR_INVALID_ARG
+    assert L.fc_chunk_select(fake, 4, 2, fake, 40, 10, fake, fake, None, fake + 8, 1.0, fake, None) == fc.FC_ERR_ALIGNMENT
+    assert L.fc_chunk_select(fake, 4, 2, fake, 40, 10, fake, fake, None, fake, float("inf"), fake, None) == fc.FC_ERR_INVALID_ARG
     # update
     assert L.fc_residual_sgd_update(fake, fake, 10, 0, 0.1, 0.9, fake, fake, fake, None, None) == fc.FC_ERR_INVALID_ARG
     assert L.fc_residual_sgd_update(fake, None, 10, 2, 0.1, 0.9, fake, fake, fake, None, None) == fc.FC_ERR_INVALID_ARG
@@ -114,9 +116,9 @@ def test_argument_errors_return_before_any_device_work(fc_lib):
     assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, fake, fake + 16, 10 ** 6, None) == fc.FC_ERR_ALIGNMENT
     assert L.fc_step_reduce(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None, None, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
     assert L.fc_step_select(16, 4, 9, fake, fake, fake, fake, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
-    assert L.fc_step_update(fake, 16, 4, 0.1, 0.9, fake, fake, fake, None, fake, fake + 4, fake, 10 ** 6, None) == fc.FC_ERR_ALIGNMENT
+    assert L.fc_step_update(fake, 16, 4, 0.1, 0.9, fake, fake, fake, None, fake, fake + 4, None, 1.0, fake, 10 ** 6, None) == fc.FC_ERR_ALIGNMENT
     assert L.fc_step(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, 5, 0.1, 0.9, fake, fake, fake, fake,
-                     None, fake, fake, fake, None, fake, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
+                     None, fake, fake, fake, None, None, 1.0, fake, fake, 10 ** 6, None) == fc.FC_ERR_INVALID_ARG
     assert b"k = 5" in L.fc_last_error()
 
 

@@ -26,7 +26,7 @@ def _lib(fc_lib):
 
 def _compare_paths(p, s):
     for key in ("a", "norms", "idx", "mask", "threshold", "residual", "velocity",
-                "weights", "packed", "w16"):
+                "weights", "packed", "packed16", "w16"):
         if key in p and key in s:
             assert bits_equal(np.asarray(p[key]), np.asarray(s[key])), key
 
@@ -235,3 +235,64 @@ def test_device_argument_errors():
     with pytest.raises(fc.FcError) as e:
         run.step(dev_grads(workload.all_grads(wl, 0)))
     assert e.value.status == fc.FC_ERR_WORKSPACE
+
+
+ORDER_CASES = [
+    (3, [1000, 7], 64),
+    (5, [17, 33, 1, 2048, 5], 100),
+    (16, [40000, 123, 70001], 4096),
+    (64, [20000], 4096),
+    (7, [3], 2),
+]
+
+
+@pytest.mark.parametrize("order", [oracle.ORDER_SEQUENTIAL, oracle.ORDER_RING])
+@pytest.mark.parametrize("case", ORDER_CASES, ids=[str(i) for i in range(len(ORDER_CASES))])
+def test_summation_orders(order, case):
+    """Parameter-server and ring orders: the materialised path and the
+    pipeline's phase 1 both match the oracle bit for bit, and the pipeline's
+    norms follow."""
+    W, sizes, chunk = case
+    wl = workload.custom(W=W, sizes=sizes, chunk=chunk, keep_percent=20,
+                         config_id=180 + W, loss_scale=1000.0)
+    g_np = workload.all_grads(wl, 0)
+    rng = np.random.default_rng(W)
+    r_np = (rng.standard_normal(wl.N) * 1e-3).astype(np.float32)
+    want = oracle.reduce_ordered(oracle.fuse_pack(g_np), wl.loss_scale, r_np, order)
+    g = dev_grads(g_np)
+    r = torch.from_numpy(r_np).cuda()
+    fused = torch.empty(W * wl.N, dtype=torch.float16, device="cuda")
+    fc.fc_fuse_pack(g, fused)
+    out = torch.empty(wl.N, dtype=torch.float32, device="cuda")
+    fc.fc_reduce_ordered(fused, W, wl.N, wl.loss_scale, r, out, order)
+    ws = torch.zeros(fc.fc_step_workspace_size(wl.N, chunk), dtype=torch.uint8, device="cuda")
+    a = torch.empty(wl.N, dtype=torch.float32, device="cuda")
+    fc.fc_step_reduce_ordered(g, wl.loss_scale, chunk, r, a, order, ws)
+    C = fc.fc_num_chunks(wl.N, chunk)
+    norms = torch.empty(C, dtype=torch.float32, device="cuda")
+    idx = torch.empty(1, dtype=torch.int32, device="cuda")
+    mask = torch.empty(C, dtype=torch.uint8, device="cuda")
+    thr = torch.empty(1, dtype=torch.float32, device="cuda")
+    fc.fc_step_select(wl.N, chunk, 1, norms, idx, mask, thr, ws)
+    torch.cuda.synchronize()
+    assert bits_equal(out.cpu().numpy(), want)
+    assert bits_equal(a.cpu().numpy(), want)
+    from tests.gpu_util import assert_close, RTOL_NORM
+    assert_close("norms", norms.cpu().numpy(), oracle.chunk_norms(want, chunk), RTOL_NORM)
+
+
+@pytest.mark.parametrize("order", [oracle.ORDER_SEQUENTIAL, oracle.ORDER_RING])
+def test_summation_orders_googlenet(order):
+    wl = workload.get("googlenet")
+    g_np = workload.all_grads(wl, 0)
+    want = oracle.reduce_ordered(oracle.fuse_pack(g_np), wl.loss_scale, None, order)
+    ws = torch.zeros(fc.fc_step_workspace_size(wl.N, wl.chunk), dtype=torch.uint8,
+                     device="cuda")
+    a = torch.empty(wl.N, dtype=torch.float32, device="cuda")
+    fc.fc_step_reduce_ordered(dev_grads(g_np), wl.loss_scale, wl.chunk, None, a, order, ws)
+    torch.cuda.synchronize()
+    assert bits_equal(a.cpu().numpy(), want)
+    # the orders differ from the tree by rounding only
+    tree = oracle.tree_reduce(oracle.fuse_pack(g_np), wl.loss_scale)
+    from tests.gpu_util import assert_close
+    assert_close("order vs tree", want, tree, 1e-5)

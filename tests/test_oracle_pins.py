@@ -166,6 +166,56 @@ def test_single_worker_is_plain_unscale():
     assert np.array_equal(a, g.astype(np.float32) / np.float32(128.0))
 
 
+# ---- a2: other summation orders --------------------------------------------------
+
+def test_sequential_order_discriminating_example():
+    x = [32768.0, 2.0 ** -10, -32768.0, 2.0 ** -10]
+    assert oracle.sequential_sum(x) == 2.0 ** -10   # (((x0+x1)+x2)+x3)
+    t = 3 * 2.0 ** -11
+    assert oracle.sequential_sum([t, t, 32768.0]) == 32768.0 + 2.0 ** -8
+    assert oracle.sequential_sum([32768.0, t, t]) == 32768.0
+
+
+def test_ring_segments_split_evenly():
+    # N = 10, W = 4: boundaries floor(s*10/4) = 0, 2, 5, 7, 10
+    assert [oracle.ring_segment(i, 10, 4) for i in range(10)] == [0, 0, 1, 1, 1, 2, 2, 3, 3, 3]
+    assert [oracle.ring_segment(i, 3, 3) for i in range(3)] == [0, 1, 2]
+    assert [oracle.ring_segment(i, 2, 5) for i in range(2)] == [2, 4]
+
+
+def test_ring_order_hand_worked():
+    # W = 3, N = 3: element i lies in segment i, so its sum starts at worker i.
+    t = 3 * 2.0 ** -11                  # 0.375 ulp of 2^15
+    big = 32768.0
+    # element 0: ((x0 + x1) + x2) with x = [big, t, t]       -> big (t lost twice)
+    # element 1: ((x1 + x2) + x0) with x = [big, t, t]       -> (2t = 0.75 ulp) + big = big + 2^-8
+    # element 2: ((x2 + x0) + x1) with x = [t, t, big]       -> (big + t) + t = big
+    col = [[big, t, t], [big, t, t], [t, t, big]]
+    fused = np.array(col, dtype=np.float16).T.copy()        # fused[w, i]
+    a = oracle.reduce_ordered(fused, 1.0, None, oracle.ORDER_RING)
+    u = oracle.unscale_factor(1.0, 3)
+    assert a[0] == np.float32(np.float32(big) * u)
+    assert a[1] == np.float32(np.float32(big + 2.0 ** -8) * u)
+    assert a[2] == np.float32(np.float32(big) * u)
+    # the same columns in parameter-server order all start at worker 0
+    s = oracle.reduce_ordered(fused, 1.0, None, oracle.ORDER_SEQUENTIAL)
+    assert s[0] == np.float32(np.float32(big) * u)
+    assert s[1] == np.float32(np.float32(big) * u)            # (big + t) + t
+    assert s[2] == np.float32(np.float32(big + 2.0 ** -8) * u)  # (t + t) + big
+    # and the tree order equals tree_reduce
+    rng = np.random.default_rng(12)
+    f = (rng.standard_normal((5, 50)) * 1000).astype(np.float16)
+    assert np.array_equal(oracle.reduce_ordered(f, 8.0, None, 0), oracle.tree_reduce(f, 8.0))
+
+
+def test_all_orders_agree_on_exact_integer_sums():
+    rng = np.random.default_rng(13)
+    vals = rng.integers(-2048, 2049, size=(7, 41))
+    f = vals.astype(np.float16)
+    outs = [oracle.reduce_ordered(f, 64.0, None, o) for o in (0, 1, 2)]
+    assert np.array_equal(outs[0], outs[1]) and np.array_equal(outs[0], outs[2])
+
+
 # ---- a3: norms ------------------------------------------------------------------
 
 def test_norm_of_constant_chunk_is_closed_form():
@@ -229,6 +279,18 @@ def test_select_packed_is_kept_chunks_zero_padded():
     assert list(mask) == [0, 1, 1]
     assert list(packed) == [5, 6, 7, 8, 9, 10, 0, 0]
     assert thr == norms[1]
+
+
+def test_fp16_send_buffer_matches_numpy_rounding():
+    rng = np.random.default_rng(11)
+    packed = np.concatenate([
+        (rng.standard_normal(5000) * np.exp(rng.uniform(-20, 12, 5000))).astype(np.float32),
+        np.float32([0.0, -0.0, 65504.0, 70000.0, 1e-9, 2.0 ** -25])])
+    for scale in (1.0, 512.0, 3.0):
+        want = (packed * np.float32(scale)).astype(np.float16).view(np.uint16)
+        assert np.array_equal(oracle.pack_fp16(packed, scale), want)
+    # hand values: 1.5 * 2 = 3 exactly; 65504 * 2 overflows to +inf
+    assert list(oracle.pack_fp16(np.float32([1.5, 65504.0, 0.0]), 2.0)) == [0x4200, 0x7c00, 0]
 
 
 def test_keep_counts_hand_worked():

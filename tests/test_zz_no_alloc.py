@@ -30,7 +30,8 @@ def _noalloc_step(run, grads):
     wl = run.wl
     fc.fc_step_noalloc(grads, wl.loss_scale, wl.chunk, run.k, wl.lr, wl.momentum,
                        run.residual, run.a, run.velocity, run.weights, run.w16, run.norms,
-                       run.idx, run.mask, run.packed, run.threshold)
+                       run.idx, run.mask, run.packed, run.threshold, None,
+                       run.packed16, run.send_scale)
 
 
 @pytest.mark.parametrize("name", ["tiny", "custom"])
@@ -50,7 +51,7 @@ def test_noalloc_matches_workspace_pipeline_on_two_calls(name):
         for key in ("a", "residual", "velocity", "weights", "norms", "threshold"):
             assert_close(key, b[key], a[key], RTOL_F32)
         for key in ("a", "residual", "velocity", "weights", "norms", "idx", "mask",
-                    "packed", "w16", "threshold"):
+                    "packed", "packed16", "w16", "threshold"):
             assert bits_equal(np.asarray(a[key]), np.asarray(b[key])), (step, key)
 
 
