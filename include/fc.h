@@ -111,7 +111,7 @@ FC_API int64_t fc_keep_count(int64_t C, int64_t keep_num, int64_t keep_den);
  * *N_out (host) = sum of the sizes.  Sizes must be >= 0 with a positive
  * sum. */
 FC_API fc_status fc_layout(int32_t L, const int64_t *sizes, int64_t *offsets,
-                    int64_t *N_out);
+                           int64_t *N_out);
 
 /* ---- a1: fuse --------------------------------------------------------------- */
 
@@ -125,8 +125,8 @@ FC_API fc_status fc_layout(int32_t L, const int64_t *sizes, int64_t *offsets,
  *           gradients.
  * W >= 1, L >= 1, W*L <= FC_MAX_TABLE_PTRS, L <= FC_MAX_TABLE_LAYERS. */
 FC_API fc_status fc_fuse_pack(const void *const *grads, int32_t W, int32_t L,
-                       const int64_t *sizes, int64_t *offsets, void *fused,
-                       void *stream);
+                              const int64_t *sizes, int64_t *offsets, void *fused,
+                              void *stream);
 
 /* ---- a2: binary-tree reduction ---------------------------------------------- */
 
@@ -136,10 +136,10 @@ FC_API fc_status fc_fuse_pack(const void *const *grads, int32_t W, int32_t L,
  *               (16-byte aligned with N % 8 == 0 takes the vector path).
  *  residual_in  device fp32 [N] or NULL (then nothing is added).
  *  out          device fp32 [N]; may alias residual_in (in place).
- * W >= 1, N >= 1, loss_scale finite and > 0. */
+ * 1 <= W <= FC_MAX_TABLE_PTRS, N >= 1, loss_scale finite and > 0. */
 FC_API fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
-                         float loss_scale, const float *residual_in,
-                         float *out, void *stream);
+                                float loss_scale, const float *residual_in,
+                                float *out, void *stream);
 
 /* Summation orders over the workers.  The engine's method is the binary
  * tree; the other two are the aggregation schemes the pages set the tree
@@ -173,7 +173,7 @@ FC_API fc_status fc_reduce_ordered(const void *fused, int32_t W, int64_t N,
  *  a      device fp32 [N].
  *  norms  device fp32 [C] output. */
 FC_API fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
-                         float *norms, void *stream);
+                                float *norms, void *stream);
 
 /* ---- a4: top-k selection and compaction -------------------------------------- */
 
@@ -209,10 +209,10 @@ FC_API fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
  *  residual, velocity, weights  device fp32 [N], updated in place.
  *  weights_fp16  device fp16 [N] output or NULL. */
 FC_API fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
-                                 int64_t N, int64_t chunk, float lr,
-                                 float momentum, float *residual,
-                                 float *velocity, float *weights,
-                                 void *weights_fp16, void *stream);
+                                        int64_t N, int64_t chunk, float lr,
+                                        float momentum, float *residual,
+                                        float *velocity, float *weights,
+                                        void *weights_fp16, void *stream);
 
 /* ---- the fused pipeline (a1..a5 without materialising the fused buffer) ---- */
 
