@@ -222,10 +222,18 @@ class ClockSampler:
 
 def kernel_source_hash():
     h = hashlib.sha256()
-    for name in ("fc_reduce.cu", "fc_common.cuh"):
+    for name in ("fc_reduce.cu", "fc_reduce_tma.cu", "fc_common.cuh"):
         with open(os.path.join(ROOT, "gradient_aggregation_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
+
+
+def phase1_kernel(wl) -> str:
+    """Which kernel phase 1 uses for this layout (mirrors the library's
+    choice: TMA staging for 4, 8 or 16 workers when every layer starts at a
+    multiple of 8 elements and the chunk is a multiple of 256)."""
+    aligned = all(s % 8 == 0 for s in wl.sizes) and wl.chunk % 256 == 0
+    return "k_reduce_tma" if wl.W in (4, 8, 16) and aligned else "k_reduce"
 
 
 def traffic_from_profile(src_hash, wl):
@@ -458,7 +466,7 @@ def run_gpu(args, wl, rank, world, local):
                       % (step_bytes / 1e9, 12 * N / 1e9)}),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "kernel": "k_reduce (fc_step_reduce)",
+                         "traffic": traffic, "kernel": "phase 1 of fc_step (%s)" % phase1_kernel(wl),
                          "algorithmic_bytes_per_launch": k_alg,
                          "avg_launch_ms": round(k_ms, 5), "peak_source": peak_src + " hbm_gbs",
                          "timed_launches": len(reduce_ms)},

@@ -150,6 +150,25 @@ fc_status check_f32(const void *p, const char *name, bool may_be_null)
     return FC_OK;
 }
 
+// The TMA-staged phase 1 serves the tree order for 4, 8 or 16 workers, when
+// the layout keeps every bulk copy 16-byte aligned.
+template <class Tab>
+bool use_tma(const Tab &tab, const UnitGeom &G, const float *partials, int order)
+{
+#ifdef FC_DISABLE_TMA
+    (void)tab; (void)G; (void)partials; (void)order;
+    return false;
+#else
+    // With more than 16 workers a 64 KB stage holds fewer than eight units,
+    // which leaves consumer warps idle; the register kernel streams those
+    // layouts at the copy rate already.
+    const int W = tab.W;
+    if (order != FC_ORDER_TREE) return false;
+    if (W != 4 && W != 8 && W != 16) return false;
+    return tma_eligible(tab, G, partials);
+#endif
+}
+
 #define TRY(x)                         \
     do {                               \
         fc_status _st = (x);           \
@@ -405,15 +424,22 @@ fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
     const UnitGeom G = ugeom(N, chunk);
     const WsLayout wl = ws_layout(N, chunk);
     float *partials = (float *)((char *)workspace + wl.partials);
+    unsigned *err = (unsigned *)((char *)workspace + wl.counters) + 1;
     cudaError_t e;
     if (fits_small(W, L)) {
         TableS tab;
         fill_table(tab, grads, W, L, sizes);
-        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
+        if (use_tma(tab, G, partials, order))
+            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream);
+        else
+            e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
     } else {
         static thread_local TableL tab;
         fill_table(tab, grads, W, L, sizes);
-        e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
+        if (use_tma(tab, G, partials, order))
+            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream);
+        else
+            e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
     }
     if (e != cudaSuccess) return cuda_fail(e, "step_reduce launch");
     return ok();
@@ -446,7 +472,7 @@ fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
     unsigned *done = (unsigned *)((char *)workspace + wl.counters);
     int32_t *slot = (int32_t *)((char *)workspace + wl.slot);
     cudaError_t e = launch_select(ugeom(N, chunk), partials, done, norms, k, idx,
-                                  mask, slot, threshold, (cudaStream_t)stream);
+                                  mask, slot, threshold, (cudaStream_t)stream, done + 1);
     if (e != cudaSuccess) return cuda_fail(e, "step_select launch");
     return ok();
 }

@@ -10,10 +10,11 @@
 //    fused index, clipped to the unit) with g = floor(lo/8) + t + 32r.
 //  * The sum of squares of a unit is the warp butterfly of the lanes' sums of
 //    their groups (each group summed pairwise).  A chunk's sum of squares is
-//    formed from its unit sums in binary64 in one fixed order: lane t adds the
-//    units j = t, t+32, t+64, ... in turn, then a butterfly over the 32 lanes.
-//    Every kernel that needs norms follows this order, so the norms are
-//    bitwise identical across the fused pipeline and the standalone calls.
+//    formed from its unit sums in float-float arithmetic in one fixed order:
+//    lane t adds the units j = t, t+32, t+64, ... in turn, then a butterfly
+//    over the 32 lanes (lane 0's result).  Every kernel that needs norms
+//    follows this order, so the norms are bitwise identical across the fused
+//    pipeline and the standalone calls.
 //  * The update works on tiles of at most FC_TILE = 2048 elements that never
 //    straddle a chunk (chunk c owns tiles c*P .. with P = ceil(cs/2048)).
 #pragma once
@@ -317,17 +318,47 @@ __device__ __forceinline__ float warp_sum_f32(float x)
     return x;
 }
 
-__device__ __forceinline__ double warp_sum_f64(double x)
+// Float-float (hi + lo) running sums: each addition keeps its exact rounding
+// error (Knuth's two-sum) in lo, so a sum of n fp32 terms is exact to about
+// n * 2^-48 relative, with fp32 instructions only (this GPU's fp64 rate is a
+// small fraction of its fp32 rate).
+struct FF {
+    float hi, lo;
+};
+
+__device__ __forceinline__ FF ff_add(FF a, float x)
+{
+    const float s = __fadd_rn(a.hi, x);
+    const float bb = __fsub_rn(s, a.hi);
+    const float err = __fadd_rn(__fsub_rn(a.hi, __fsub_rn(s, bb)), __fsub_rn(x, bb));
+    return FF{s, __fadd_rn(a.lo, err)};
+}
+
+__device__ __forceinline__ FF ff_add(FF a, FF b)
+{
+    FF r = ff_add(a, b.hi);
+    r.lo = __fadd_rn(r.lo, b.lo);
+    return r;
+}
+
+// Butterfly over the 32 lanes; lane 0's result is the defined one.
+__device__ __forceinline__ FF warp_sum_ff(FF x)
 {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        x = __dadd_rn(x, __shfl_xor_sync(0xffffffffu, x, o));
+    for (int o = 16; o > 0; o >>= 1) {
+        FF y;
+        y.hi = __shfl_xor_sync(0xffffffffu, x.hi, o);
+        y.lo = __shfl_xor_sync(0xffffffffu, x.lo, o);
+        x = ff_add(x, y);
+    }
     return x;
 }
 
-__device__ __forceinline__ float norm_from_sumsq(double ss)
+// Norm of a chunk from its float-float sum of squares: hi + lo rounded to
+// fp32, then the correctly rounded fp32 square root.
+__device__ __forceinline__ float norm_from_sumsq(FF ss)
 {
-    return __double2float_rn(__dsqrt_rn(ss));
+    return __fsqrt_rn(__fadd_rn(ss.hi, ss.lo));
 }
 
 }  // namespace fc

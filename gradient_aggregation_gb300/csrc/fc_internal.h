@@ -21,6 +21,15 @@ cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
                           const float *resid, float *out, float *partials,
                           cudaStream_t s, int order = 0);
 
+// TMA-staged phase 1 (tree order only).  tma_eligible: the layout and W
+// allow it; err: a device word set if a wait inside the kernel gave up.
+template <class Tab>
+bool tma_eligible(const Tab &tab, const UnitGeom &G, const float *partials);
+template <class Tab>
+cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
+                              const float *resid, float *out, float *partials,
+                              unsigned *err, cudaStream_t s);
+
 template <class Tab>
 cudaError_t launch_pack(const Tab &tab, int64_t N, __half *fused,
                         cudaStream_t s);
@@ -35,7 +44,8 @@ cudaError_t launch_norms(const float *a, const UnitGeom &G, float *norms,
 cudaError_t launch_select(const UnitGeom &G, const float *partials,
                           unsigned *done, float *norms, int64_t k,
                           int32_t *idx, uint8_t *mask, int32_t *slot,
-                          float *threshold, cudaStream_t s);
+                          float *threshold, cudaStream_t s,
+                          unsigned *err = nullptr);
 
 cudaError_t launch_gather(const float *a, int64_t N, int64_t cs, int64_t P,
                           const int32_t *idx, int64_t k, float *packed,

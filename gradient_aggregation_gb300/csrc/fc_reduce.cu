@@ -104,10 +104,16 @@ int grid_for(const void *kernel, int block, size_t smem, int64_t work)
 // `partials` given, the warp also writes the unit's sum of squares, which
 // the selection kernel turns into chunk norms.
 
+// Resident blocks per SM the register allocation aims at for W <= 16.
+#ifndef FC_REDUCE_MIN_BLOCKS_SMALL_W
+#define FC_REDUCE_MIN_BLOCKS_SMALL_W 3
+#endif
+
 // ORDER: 0 the binary tree, 1 parameter server (workers in index order),
 // 2 ring reduce-scatter (see fc_common.cuh).
 template <class Tab, int WT, int MAXH, int ORDER>
-__global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0 && WT <= 16) ? 3 : 2))
+__global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1
+                                            : ((WT > 0 && WT <= 16) ? FC_REDUCE_MIN_BLOCKS_SMALL_W : 2))
     k_reduce(const __grid_constant__ Tab tab, const UnitGeom G, const float u,
              const float *resid, float *out, float *partials)
 {
@@ -115,6 +121,9 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1 : ((WT > 0
     const int W = WT > 0 ? WT : tab.W;
     const int L = tab.L;
     const int lane = threadIdx.x & 31;
+    // Launched after whatever the stream ran before (programmatic serialisation):
+    // nothing is read before that work is complete.
+    wait_for_prior_grid();
     allow_dependent_launch();  // the selection may be scheduled; it waits for us
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
 
@@ -203,8 +212,8 @@ static cudaError_t launch_reduce_w(const Tab &tab, const UnitGeom &G, float u,
     auto kern = k_reduce<Tab, WT, MAXH, ORDER>;
     const int64_t blocks_needed = (G.units + FC_BLOCK / 32 - 1) / (FC_BLOCK / 32);
     const int grid = grid_for((const void *)kern, FC_BLOCK, 0, blocks_needed);
-    kern<<<grid, FC_BLOCK, 0, s>>>(tab, G, u, resid, out, partials);
-    return cudaGetLastError();
+    return launch_after_prior(kern, (unsigned)grid, FC_BLOCK, 0, s, tab, G, u, resid,
+                              out, partials);
 }
 
 template <class Tab>

@@ -26,20 +26,20 @@ namespace fc {
 // ---- a3 ------------------------------------------------------------------------
 
 // One block of 8 warps per chunk.  Warp w forms the sums of the units
-// j = w, w+8, w+16, ... of the chunk exactly as the reduction kernel does, and
-// keeps four binary64 running sums, one per residue class j mod 32 it sees
-// (w, w+8, w+16, w+24), added in increasing j.  Those 32 class sums then go
-// through the same binary64 butterfly as the reduction kernel's chunk
-// finish, so both produce the same bits.
+// j = w, w+8, w+16, ... of the chunk exactly as the reduction kernels do, and
+// keeps four float-float running sums, one per residue class j mod 32 it
+// sees (w, w+8, w+16, w+24), added in increasing j.  Those 32 class sums then
+// go through the same butterfly as the selection kernel's chunk finish, so
+// both produce the same bits.
 __global__ void __launch_bounds__(FC_BLOCK)
     k_norms(const float *__restrict__ a, const UnitGeom G,
             float *__restrict__ norms)
 {
-    __shared__ double res[32];
+    __shared__ float res_hi[32], res_lo[32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     for (int64_t c = blockIdx.x; c < G.C; c += gridDim.x) {
         const int64_t Uc = units_of_chunk(G, c);
-        double acc[4] = {0.0, 0.0, 0.0, 0.0};
+        FF acc[4] = {{0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}, {0.f, 0.f}};
         for (int64_t base = 0; base < Uc; base += 32) {
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
@@ -67,16 +67,19 @@ __global__ void __launch_bounds__(FC_BLOCK)
                     tss = __fadd_rn(tss, group_sumsq(v));
                 }
                 tss = warp_sum_f32(tss);
-                acc[q] = __dadd_rn(acc[q], (double)tss);
+                acc[q] = ff_add(acc[q], tss);
             }
         }
         if (lane == 0) {
 #pragma unroll
-            for (int q = 0; q < 4; ++q) res[warp + 8 * q] = acc[q];
+            for (int q = 0; q < 4; ++q) {
+                res_hi[warp + 8 * q] = acc[q].hi;
+                res_lo[warp + 8 * q] = acc[q].lo;
+            }
         }
         __syncthreads();
         if (warp == 0) {
-            const double ss = warp_sum_f64(res[lane]);
+            const FF ss = warp_sum_ff(FF{res_hi[lane], res_lo[lane]});
             if (lane == 0) norms[c] = norm_from_sumsq(ss);
         }
         __syncthreads();
@@ -126,17 +129,17 @@ __device__ __forceinline__ uint64_t block_excl_scan64(uint64_t x, uint64_t *sw,
 }
 
 // Chunk norm from the unit sums, in the fixed order (see fc_common.cuh):
-// lane t adds units t, t+32, ... in binary64, then a binary64 butterfly.
-// Called by a whole warp; the result is valid in every lane.
+// lane t adds units t, t+32, ... in float-float arithmetic, then the
+// butterfly.  Called by a whole warp; the result is valid in lane 0.
 __device__ __forceinline__ float chunk_norm_from_units(const UnitGeom &G,
                                                        const float *partials,
                                                        int64_t c, int lane)
 {
     const int64_t Uc = units_of_chunk(G, c);
-    double ss = 0.0;
+    FF ss = {0.f, 0.f};
     for (int64_t j = lane; j < Uc; j += 32)
-        ss = __dadd_rn(ss, (double)__ldcg(partials + c * G.U + j));
-    return norm_from_sumsq(warp_sum_f64(ss));
+        ss = ff_add(ss, __ldcg(partials + c * G.U + j));
+    return norm_from_sumsq(warp_sum_ff(ss));
 }
 
 // Selection kernel.  With partials != NULL every block first turns the unit
@@ -155,7 +158,8 @@ __global__ void __launch_bounds__(SEL_THREADS)
     k_select(const UnitGeom G, const float *__restrict__ partials,
              unsigned *__restrict__ done, float *norms, const int64_t k,
              int32_t *__restrict__ idx, uint8_t *__restrict__ mask,
-             int32_t *__restrict__ slot, float *__restrict__ threshold)
+             int32_t *__restrict__ slot, float *__restrict__ threshold,
+             unsigned *__restrict__ err)
 {
     __shared__ uint32_t skeys[SEL_SMEM_KEYS];
     __shared__ uint32_t hist[256];
@@ -183,6 +187,21 @@ __global__ void __launch_bounds__(SEL_THREADS)
         if (!s_last) return;
         __threadfence();
         if (tid == 0) *done = 0u;  // ready for the next call
+        // A wait inside the staged reduction gave up (not expected to
+        // happen): report it as a NaN threshold with nothing kept.
+        if (err && __ldcg(err) != 0u) {
+            for (int64_t c = tid; c < C; c += SEL_THREADS) {
+                mask[c] = 0;
+                if (slot) slot[c] = -1;
+            }
+            for (int64_t q = tid; q < k; q += SEL_THREADS) idx[q] = -1;
+            __syncthreads();
+            if (tid == 0) {
+                threshold[0] = __int_as_float(0x7fc00000);
+                *err = 0u;
+            }
+            return;
+        }
     }
 
     const bool in_smem = C <= SEL_SMEM_KEYS;
@@ -282,7 +301,7 @@ __global__ void __launch_bounds__(SEL_THREADS)
 cudaError_t launch_select(const UnitGeom &G, const float *partials,
                           unsigned *done, float *norms, int64_t k,
                           int32_t *idx, uint8_t *mask, int32_t *slot,
-                          float *threshold, cudaStream_t s)
+                          float *threshold, cudaStream_t s, unsigned *err)
 {
     int64_t blocks = 1;
     if (partials) {
@@ -291,7 +310,8 @@ cudaError_t launch_select(const UnitGeom &G, const float *partials,
         if (blocks > cap) blocks = cap;  // all blocks resident: no queueing
     }
     return launch_after_prior(k_select, (unsigned)blocks, SEL_THREADS, 0, s, G,
-                              partials, done, norms, k, idx, mask, slot, threshold);
+                              partials, done, norms, k, idx, mask, slot, threshold,
+                              err);
 }
 
 // ---- packed copy of the kept chunks ----------------------------------------------

@@ -42,6 +42,7 @@ __global__ void __launch_bounds__(FC_BLOCK)
     const int64_t cs = G.cs;
     const bool pvec = (cs & 3) == 0;
     wait_for_prior_grid();
+    allow_dependent_launch();  // the next step's reduction waits for us
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         int64_t lo, hi, c, hin;
         const bool any = tile_range(G, t, lo, hi, c, hin);

@@ -167,9 +167,11 @@ FC_API fc_status fc_reduce_ordered(const void *fused, int32_t W, int64_t N,
 
 /* norms[c] = sqrt(sum_{i in chunk c} a[i]^2), c < C = fc_num_chunks(N, chunk).
  * Squares and partial sums in fp32 over units of at most 256 elements
- * (pairs of 8, then a warp butterfly), the unit sums added in fp64 in a
- * fixed order; the relative error is below 6e-7.  Deterministic: the same
- * inputs give the same bits, and the same bits as fc_step_reduce.
+ * (pairs of 8, then a warp butterfly), the unit sums added in float-float
+ * (compensated fp32) arithmetic in a fixed order, then a correctly rounded
+ * fp32 square root; the relative error is below 6e-7.  Deterministic: the
+ * same inputs give the same bits, and the same bits as the pipeline's
+ * fc_step_select.
  *  a      device fp32 [N].
  *  norms  device fp32 [C] output. */
 FC_API fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
