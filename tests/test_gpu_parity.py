@@ -296,3 +296,45 @@ def test_summation_orders_googlenet(order):
     tree = oracle.tree_reduce(oracle.fuse_pack(g_np), wl.loss_scale)
     from tests.gpu_util import assert_close
     assert_close("order vs tree", want, tree, 1e-5)
+
+
+def test_engine_phase_calls_equal_fused_step():
+    """The three phase entry points in sequence are fc_step; Engine state
+    round-trips through state_dict."""
+    wl = workload.custom(W=16, sizes=[8192, 4096, 24576], chunk=2048, keep_percent=25,
+                         config_id=190, steps=2)
+    w0 = torch.from_numpy(workload.initial_weights(wl)).cuda()
+    engines = [fc.Engine(wl.sizes, wl.W, wl.chunk, wl.keep_percent, 100, wl.loss_scale,
+                         wl.lr, wl.momentum, w0, want_fp16=True, want_packed_fp16=True,
+                         send_scale=wl.loss_scale) for _ in range(2)]
+    for s in range(2):
+        table = fc.PtrTable(dev_grads(workload.all_grads(wl, s)))
+        engines[0].step(table)
+        for phase in engines[1].phases(table):
+            phase()
+    torch.cuda.synchronize()
+    a, b = engines
+    for name in ("residual", "velocity", "weights", "weights_fp16", "norms", "idx", "mask",
+                 "packed", "packed_fp16", "threshold"):
+        assert torch.equal(getattr(a, name), getattr(b, name)), name
+    sd = a.state_dict()
+    c = fc.Engine(wl.sizes, wl.W, wl.chunk, wl.keep_percent, 100, wl.loss_scale, wl.lr,
+                  wl.momentum, w0)
+    c.load_state_dict(sd)
+    assert torch.equal(c.weights, a.weights) and torch.equal(c.residual, a.residual)
+
+
+def test_tree_order_entry_points_agree():
+    wl = workload.custom(W=8, sizes=[3000, 5000], chunk=512, keep_percent=10, config_id=191)
+    g = dev_grads(workload.all_grads(wl, 0))
+    fused = torch.empty(wl.W * wl.N, dtype=torch.float16, device="cuda")
+    fc.fc_fuse_pack(g, fused)
+    outs = [torch.empty(wl.N, dtype=torch.float32, device="cuda") for _ in range(4)]
+    fc.fc_tree_reduce(fused, wl.W, wl.N, wl.loss_scale, None, outs[0])
+    fc.fc_reduce_ordered(fused, wl.W, wl.N, wl.loss_scale, None, outs[1], fc.FC_ORDER_TREE)
+    ws = torch.zeros(fc.fc_step_workspace_size(wl.N, wl.chunk), dtype=torch.uint8, device="cuda")
+    fc.fc_step_reduce(g, wl.loss_scale, wl.chunk, None, outs[2], ws)
+    fc.fc_step_reduce_ordered(g, wl.loss_scale, wl.chunk, None, outs[3], fc.FC_ORDER_TREE, ws)
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
