@@ -15,6 +15,7 @@
 // Every wait on an mbarrier gives up after a time limit (read from the
 // global timer); the kernel then records the failure in `err` and returns,
 // the producer first waiting (again with a limit) for the copies it issued.
+#include <atomic>
 #include <mutex>
 
 #include "fc_internal.h"
@@ -84,17 +85,25 @@ __device__ __forceinline__ void bulk_g2s(uint32_t dst, const void *src, uint32_t
         : "memory");
 }
 
+// Test hook (fc_test_stage_loss): a one-shot tile to drop and the wait limit
+// that goes with it.
+std::atomic<int64_t> g_drop_tile{-1};
+std::atomic<uint64_t> g_drop_limit_ns{0};
+
 constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any tile
 
 }  // namespace
 
+// drop_tile >= 0 (test hook only, see fc_test_stage_loss): the producer
+// issues no copies for that tile, so the bounded waits on it run out.
 template <class Tab, int WT, int MAXH>
 __global__ void __launch_bounds__(kThreads, 1)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
-                 float *partials, unsigned *err)
+                 float *partials, unsigned *err, const int64_t drop_tile,
+                 const uint64_t limit_ns)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
@@ -126,10 +135,11 @@ __global__ void __launch_bounds__(kThreads, 1)
         int it = 0;
         for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const int s = it % S;
-            if (it >= S && !mbar_wait(smem_u32(&bars[S + s]), ((it / S) - 1) & 1, kWaitLimitNs)) {
+            if (it >= S && !mbar_wait(smem_u32(&bars[S + s]), ((it / S) - 1) & 1, limit_ns)) {
                 atomicOr(err, 1u);
                 break;
             }
+            if (t == drop_tile) continue;
             const int64_t f0 = t * TT;
             const int64_t f1 = f0 + TT < N ? f0 + TT : N;
             const uint32_t full = smem_u32(&bars[s]);
@@ -146,12 +156,12 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             if (resid) bulk_g2s(smem_u32(st + gbytes), resid + f0, (uint32_t)((f1 - f0) * 4), full);
         }
-        // no copy may still be landing in shared memory when the CTA exits
+        // No copy may still be landing in shared memory when the CTA exits:
+        // wait for every stage still in flight (each wait bounded; a stage
+        // that gives up does not stop the waits for the others).
         for (int j = it > S ? it - S : 0; j < it; ++j)
-            if (!mbar_wait(smem_u32(&bars[j % S]), (j / S) & 1, kWaitLimitNs)) {
+            if (!mbar_wait(smem_u32(&bars[j % S]), (j / S) & 1, limit_ns))
                 atomicOr(err, 2u);
-                break;
-            }
         return;
     }
 
@@ -159,7 +169,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
         const int s = it % S;
-        if (!mbar_wait(smem_u32(&bars[s]), (it / S) & 1, kWaitLimitNs)) {
+        if (!mbar_wait(smem_u32(&bars[s]), (it / S) & 1, limit_ns)) {
             if (lane == 0) atomicOr(err, 4u);
             return;
         }
@@ -259,8 +269,10 @@ static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
     }
     const int64_t tiles = (G.N + TT - 1) / TT;
     const int grid = grid_for((const void *)kern, kThreads, smem, tiles);
+    const int64_t drop = g_drop_tile.exchange(-1);
+    const uint64_t limit = drop >= 0 ? g_drop_limit_ns.load() : kWaitLimitNs;
     return launch_after_prior(kern, (unsigned)grid, kThreads, smem, s, tab, G, TT, S, u,
-                              resid, out, partials, err);
+                              resid, out, partials, err, drop, limit);
 }
 
 template <class Tab>
@@ -276,6 +288,19 @@ cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
     }
     return cudaErrorNotSupported;
 }
+
+}  // namespace fc
+
+extern "C" fc_status fc_test_stage_loss(int64_t tile, uint64_t wait_limit_ns)
+{
+    if (tile >= 0 && (wait_limit_ns < 1000000ull || wait_limit_ns > 2000000000ull))
+        return fc::set_error(FC_ERR_INVALID_ARG, "wait_limit_ns must be in [1 ms, 2 s]");
+    fc::g_drop_limit_ns.store(wait_limit_ns);
+    fc::g_drop_tile.store(tile < 0 ? -1 : tile);
+    return FC_OK;
+}
+
+namespace fc {
 
 template bool tma_eligible<TableS>(const TableS &, const UnitGeom &, const float *);
 template bool tma_eligible<TableL>(const TableL &, const UnitGeom &, const float *);

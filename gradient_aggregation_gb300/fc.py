@@ -51,6 +51,7 @@ _SIGS = {
                                        _P, _P]),
     "fc_residual_sgd_update": (ctypes.c_int, [_P, _P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P]),
     "fc_step_workspace_size": (_SZ, [_I64, _I64]),
+    "fc_test_stage_loss": (ctypes.c_int, [_I64, ctypes.c_uint64]),
     "fc_step_reduce": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _P, _SZ, _P]),
     "fc_step_select": (ctypes.c_int, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "fc_step_update": (ctypes.c_int, [_P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P, _P, _P,
@@ -167,6 +168,12 @@ def fc_layout(sizes: Sequence[int]) -> Tuple[List[int], int]:
 
 def fc_step_workspace_size(N: int, chunk: int) -> int:
     return int(lib().fc_step_workspace_size(int(N), int(chunk)))
+
+
+def fc_test_stage_loss(tile: int, wait_limit_ns: int = 20_000_000) -> None:
+    """Test hook: the next TMA-staged reduction drops the copies of `tile`
+    and bounds its waits by wait_limit_ns (see include/fc.h)."""
+    _check(lib().fc_test_stage_loss(int(tile), int(wait_limit_ns)))
 
 
 # ---- the five calls ---------------------------------------------------------------

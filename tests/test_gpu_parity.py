@@ -338,3 +338,67 @@ def test_tree_order_entry_points_agree():
     torch.cuda.synchronize()
     for o in outs[1:]:
         assert torch.equal(o, outs[0])
+
+
+def test_capacity_limits_many_workers_and_layers():
+    """The largest pointer tables one call accepts: W*L = FC_MAX_TABLE_PTRS
+    (3072 workers of one layer; 6 workers of 512 layers)."""
+    for W, sizes, chunk in ((fc.FC_MAX_TABLE_PTRS, [24], 8),
+                            (6, [1 + (i * 7) % 13 for i in range(fc.FC_MAX_TABLE_LAYERS)], 64)):
+        wl = workload.custom(W=W, sizes=sizes, chunk=chunk, keep_percent=30,
+                             config_id=200 + (W % 100), loss_scale=4096.0)
+        _run_workload(wl, steps=1, both_paths=True)
+
+
+def test_more_chunks_than_the_select_kernel_keeps_in_shared_memory():
+    """C = 12,000 chunks of one element (above the 11,264 keys the selection
+    holds in shared memory): the keys are read from global memory."""
+    wl = workload.custom(W=3, sizes=[12000], chunk=1, keep_percent=10, config_id=210)
+    _run_workload(wl, steps=2)
+
+
+def test_select_with_only_the_fp16_send_buffer():
+    wl = workload.custom(W=4, sizes=[5000], chunk=100, keep_percent=20, config_id=211)
+    g_np = workload.all_grads(wl, 0)
+    a_np = oracle.tree_reduce(oracle.fuse_pack(g_np), wl.loss_scale)
+    norms_np = oracle.chunk_norms(a_np, wl.chunk)
+    k = oracle.keep_count(norms_np.size, wl.keep_percent, 100)
+    idx_o, mask_o, packed_o, thr_o = oracle.chunk_select(norms_np, k, a_np, wl.chunk)
+    a = torch.from_numpy(a_np).cuda()
+    norms = torch.from_numpy(norms_np).cuda()
+    idx = torch.empty(k, dtype=torch.int32, device="cuda")
+    mask = torch.empty(norms_np.size, dtype=torch.uint8, device="cuda")
+    thr = torch.empty(1, dtype=torch.float32, device="cuda")
+    p16 = torch.empty(k * wl.chunk, dtype=torch.float16, device="cuda")
+    fc.fc_chunk_select(norms, norms_np.size, k, a, wl.N, wl.chunk, idx, mask, None, thr,
+                       packed_fp16=p16, send_scale=wl.loss_scale)
+    torch.cuda.synchronize()
+    assert np.array_equal(idx.cpu().numpy(), idx_o)
+    assert np.array_equal(mask.cpu().numpy(), mask_o)
+    assert bits_equal(p16.cpu().numpy().view(np.uint16), oracle.pack_fp16(packed_o, wl.loss_scale))
+
+
+def test_staged_reduction_reports_a_wait_that_runs_out():
+    """Failure path of the TMA-staged reduction, without any fault: the test
+    hook makes the next launch issue no copies for tile 0, so the waits on it
+    run out (20 ms limit).  The step reports it (NaN threshold, nothing kept,
+    idx -1), the context stays usable, and the next steps match the oracle."""
+    wl = workload.custom(W=16, sizes=[8192, 16384, 40960], chunk=4096, keep_percent=25,
+                         config_id=220, steps=2)
+    run = GpuRun(wl, "pipeline", inplace=True)
+    g0 = dev_grads(workload.all_grads(wl, 0))
+    fc.fc_test_stage_loss(0, 20_000_000)
+    run.step(g0)
+    snap = run.snapshot()
+    assert np.isnan(snap["threshold"])
+    assert not snap["mask"].any() and np.all(snap["idx"] == -1)
+    # the context is usable: restart from a known state and compare
+    run2 = GpuRun(wl, "pipeline", inplace=True)
+    st = oracle.State(workload.initial_weights(wl))
+    for s in range(2):
+        g_np = workload.all_grads(wl, s)
+        run2.step(dev_grads(g_np))
+        oracle_step(g_np, st, wl, run2.snapshot(), check_a=False)
+    # the failed engine's own workspace recovers too: its next threshold is finite
+    run.step(g0)
+    assert np.isfinite(run.snapshot()["threshold"])
