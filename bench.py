@@ -312,7 +312,8 @@ def run_gpu(args, wl, rank, world, local):
         phases[2]()
 
     torch.cuda.synchronize()
-    for _ in range(max(3, args.warmup)):
+    warmup = max(3, args.warmup)   # at least three untimed steps
+    for _ in range(warmup):
         step_phased()
     torch.cuda.synchronize()
 
@@ -471,7 +472,7 @@ def run_gpu(args, wl, rank, world, local):
     if rank == 0:
         line = {
             "metric": METRIC, "value": round(value, 3), "unit": UNIT, "n_gpus": world,
-            "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "steps": K, "warmup": warmup, "ms_per_step": round(ms_per_step, 5),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
             "dtype": "f32", "data": "synthetic (seeded Gaussian fp16 gradients, workload-shaped)",
             "config": config_of(wl, {

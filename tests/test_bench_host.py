@@ -64,3 +64,15 @@ def test_reference_arm_line_and_other_ranks():
     env.update(RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
     out = subprocess.run(cmd, capture_output=True, text=True, env=env, timeout=600)
     assert out.returncode == 0 and out.stdout.strip() == ""
+
+
+def test_phase1_kernel_choice_and_profile_parsing():
+    from gradient_aggregation_gb300 import workload
+    assert bench.phase1_kernel(workload.get("alexnet")) == "k_reduce_tma"
+    assert bench.phase1_kernel(workload.get("stress")) == "k_reduce"      # 64 workers
+    assert bench.phase1_kernel(workload.get("googlenet")) == "k_reduce"   # misaligned layers
+    wl = workload.get("alexnet")
+    # the committed summary is used only for the kernel source it was taken on
+    assert bench.traffic_from_profile("not-the-current-source", wl) is None
+    t = bench.traffic_from_profile(bench.kernel_source_hash(), wl)
+    assert t is None or 2.0e9 < t < 3.0e9
