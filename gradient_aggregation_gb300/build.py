@@ -86,7 +86,7 @@ def build_library(force: bool = False, verbose: bool = False) -> str:
         if rc != 0:
             raise RuntimeError("nvcc failed: " + " ".join(cmd))
     tmp = LIB_PATH + ".tmp.%d" % os.getpid()
-    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs]
+    link = [nvcc, *ARCH, "-shared", "-cudart", "static", "-o", tmp, *objs, "-ldl"]
     p = subprocess.run(link, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
     if p.returncode != 0:
         sys.stderr.write(p.stdout)

@@ -6,12 +6,22 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "fc.h"
 #include "fc_internal.h"
 
 using namespace fc;
 
 namespace {
+
+// NVTX range around every entry point (a no-op unless a profiler such as
+// Nsight Systems or Nsight Compute is attached), so that traces show the
+// engine's calls by name.
+struct TraceRange {
+    explicit TraceRange(const char *name) { nvtxRangePushA(name); }
+    ~TraceRange() { nvtxRangePop(); }
+};
 
 thread_local char g_err[512] = "";
 
@@ -193,7 +203,9 @@ int64_t fc_keep_count(int64_t C, int64_t keep_num, int64_t keep_den)
 {
     if (C < 1 || keep_num < 0 || keep_den < 1) return -1;
     if (keep_num > keep_den) keep_num = keep_den;
-    int64_t k = ceil_div(C * keep_num, keep_den);
+    // C * keep_num may not fit in 64 bits for large denominators
+    const __int128 prod = (__int128)C * keep_num;
+    int64_t k = (int64_t)((prod + keep_den - 1) / keep_den);
     if (k < 1) k = 1;
     if (k > C) k = C;
     return k;
@@ -219,6 +231,7 @@ fc_status fc_fuse_pack(const void *const *grads, int32_t W, int32_t L,
                        const int64_t *sizes, int64_t *offsets, void *fused,
                        void *stream)
 {
+    TraceRange trace("fc_fuse_pack");
     int64_t N = 0;
     TRY(check_sizes(L, sizes, &N));
     TRY(check_table(grads, W, L, sizes));
@@ -244,6 +257,7 @@ fc_status fc_reduce_ordered(const void *fused, int32_t W, int64_t N,
                             float loss_scale, const float *residual_in,
                             float *out, int32_t order, void *stream)
 {
+    TraceRange trace("fc_reduce_ordered");
     if (order < FC_ORDER_TREE || order > FC_ORDER_RING)
         return fail(FC_ERR_INVALID_ARG, "order = %d is not an FC_ORDER_* value", order);
     if (!fused) return fail(FC_ERR_INVALID_ARG, "fused is NULL");
@@ -289,6 +303,7 @@ fc_status fc_tree_reduce(const void *fused, int32_t W, int64_t N,
 fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
                          float *norms, void *stream)
 {
+    TraceRange trace("fc_chunk_norms");
     if (N < 1) return fail(FC_ERR_INVALID_ARG, "N must be >= 1");
     if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
     TRY(check_f32(a, "a", false));
@@ -318,6 +333,7 @@ fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
                           void *packed_fp16, float send_scale,
                           float *threshold, void *stream)
 {
+    TraceRange trace("fc_chunk_select");
     TRY(check_select_args(C, k, idx, mask, threshold));
     TRY(check_f32(norms, "norms", false));
     if (packed || packed_fp16) {
@@ -372,6 +388,7 @@ fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
                                  float *velocity, float *weights,
                                  void *weights_fp16, void *stream)
 {
+    TraceRange trace("fc_residual_sgd_update");
     TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
                           weights, weights_fp16));
     TRY(bind_device(stream, a));
@@ -408,6 +425,7 @@ fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
                                  int32_t order, void *workspace,
                                  size_t workspace_bytes, void *stream)
 {
+    TraceRange trace("fc_step_reduce_ordered");
     if (order < FC_ORDER_TREE || order > FC_ORDER_RING)
         return fail(FC_ERR_INVALID_ARG, "order = %d is not an FC_ORDER_* value", order);
     int64_t N = 0;
@@ -461,6 +479,7 @@ fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
                          void *workspace, size_t workspace_bytes,
                          void *stream)
 {
+    TraceRange trace("fc_step_select");
     if (N < 1 || chunk < 1) return fail(FC_ERR_INVALID_ARG, "N and chunk must be >= 1");
     const int64_t C = ceil_div(N, chunk);
     TRY(check_select_args(C, k, idx, mask, threshold));
@@ -484,6 +503,7 @@ fc_status fc_step_update(const float *a, int64_t N, int64_t chunk, float lr,
                          void *packed_fp16, float send_scale, void *workspace,
                          size_t workspace_bytes, void *stream)
 {
+    TraceRange trace("fc_step_update");
     TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
                           weights, weights_fp16));
     TRY(check_f32(packed, "packed", true));
@@ -512,6 +532,7 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                   float send_scale, float *threshold, void *workspace,
                   size_t workspace_bytes, void *stream)
 {
+    TraceRange trace("fc_step");
     int64_t N = 0;
     TRY(check_sizes(L, sizes, &N));
     // check everything before the first launch so that an error launches

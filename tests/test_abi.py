@@ -42,6 +42,8 @@ def test_num_chunks_and_keep_counts(fc_lib):
     assert fc.fc_keep_count(10, 0, 100) == 1
     assert fc.fc_keep_count(10, 250, 100) == 10
     assert fc.fc_keep_count(0, 1, 1) == -1
+    # no overflow of C * keep_num for a large denominator: ceil(4096 * 10^17 / 10^18) = 410
+    assert fc.fc_keep_count(4096, 10 ** 17, 10 ** 18) == 410
 
 
 def test_layout_matches_hand_worked_offsets(fc_lib):
