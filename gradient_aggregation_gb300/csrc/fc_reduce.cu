@@ -21,6 +21,12 @@
 
 namespace fc {
 
+// Builds the kernels' layer table.  Consecutive layers that lie back to
+// back in memory for every worker (a gradient bucket) are merged into one
+// segment: the layout of the fused vector is the same, the kernels just see
+// fewer, longer layers (and a bucketed layout with odd layer sizes becomes
+// one aligned segment per worker).  Empty layers contribute nothing and are
+// dropped.
 template <class Tab>
 bool fill_table(Tab &t, const void *const *grads, int32_t W, int32_t L,
                 const int64_t *sizes)
@@ -28,25 +34,46 @@ bool fill_table(Tab &t, const void *const *grads, int32_t W, int32_t L,
     const int maxp = (int)(sizeof(t.ptr) / sizeof(t.ptr[0]));
     const int maxl = (int)(sizeof(t.off) / sizeof(t.off[0])) - 1;
     if (L > maxl || (int64_t)W * L > maxp) return false;
-    t.W = W;
-    t.L = L;
-    int64_t acc = 0;
+    // first pass: segment boundaries
+    static thread_local int seg_first[FC_MAX_TABLE_LAYERS + 1];
+    int nseg = 0;
+    int64_t seg_len = 0;
+    int prev = -1;
     for (int l = 0; l < L; ++l) {
-        t.off[l] = acc;
+        if (sizes[l] == 0) continue;
+        bool extend = prev >= 0;
+        for (int w = 0; extend && w < W; ++w) {
+            const char *end = (const char *)grads[(int64_t)w * L + prev] + 2 * seg_len;
+            if ((const char *)grads[(int64_t)w * L + l] != end) extend = false;
+        }
+        if (extend) {
+            seg_len += sizes[l];
+        } else {
+            seg_first[nseg++] = l;
+            prev = l;
+            seg_len = sizes[l];
+        }
+    }
+    t.W = W;
+    t.L = nseg;
+    // fused offsets of the segments
+    int64_t acc = 0;
+    int seg = 0;
+    for (int l = 0; l < L; ++l) {
+        if (seg < nseg && seg_first[seg] == l) t.off[seg++] = acc;
         acc += sizes[l];
     }
-    t.off[L] = acc;
+    t.off[nseg] = acc;
     for (int i = 0; i < (maxl + 31) / 32; ++i) t.vec[i] = 0;
-    for (int l = 0; l < L; ++l) {
+    for (int sg = 0; sg < nseg; ++sg) {
         bool ok = true;
         for (int w = 0; w < W; ++w) {
-            uintptr_t p = (uintptr_t)grads[(int64_t)w * L + l];
-            if ((p - 2u * (uintptr_t)t.off[l]) & 15u) ok = false;
+            uintptr_t p = (uintptr_t)grads[(int64_t)w * L + seg_first[sg]];
+            if ((p - 2u * (uintptr_t)t.off[sg]) & 15u) ok = false;
+            t.ptr[w * nseg + sg] = static_cast<const __half *>(grads[(int64_t)w * L + seg_first[sg]]);
         }
-        if (ok) t.vec[l >> 5] |= 1u << (l & 31);
+        if (ok) t.vec[sg >> 5] |= 1u << (sg & 31);
     }
-    for (int64_t i = 0; i < (int64_t)W * L; ++i)
-        t.ptr[i] = static_cast<const __half *>(grads[i]);
     return true;
 }
 

@@ -8,10 +8,10 @@
 //
 // GB300 mapping:
 //  * norms: one block per chunk forms the chunk's unit sums with the same
-//    warp/lane mapping and the same binary64 order as the fused reduction
+//    warp/lane mapping and the same float-float order as the fused reduction
 //    kernel, so both produce the same bits;
 //  * select: in the pipeline, blocks of 32 warps first turn the reduction's
-//    unit sums into chunk norms (one warp per chunk, the fixed binary64
+//    unit sums into chunk norms (one warp per chunk, the fixed float-float
 //    order); the last block to finish then selects.  C is at most a few
 //    thousand, so one 1024-thread block holds the norms in shared memory and
 //    runs a 4-pass radix select (8 bits a pass) on their bit patterns, then

@@ -402,3 +402,32 @@ def test_staged_reduction_reports_a_wait_that_runs_out():
     # the failed engine's own workspace recovers too: its next threshold is finite
     run.step(g0)
     assert np.isfinite(run.snapshot()["threshold"])
+
+
+def test_bucketed_gradients_merge_into_one_segment():
+    """Each worker's layers back to back in one bucket (odd layer sizes):
+    the table merges them, the staged reduction applies, and the results are
+    those of separately allocated layer tensors, bit for bit."""
+    wl = workload.custom(W=16, sizes=[1001, 33, 4099, 7, 60000, 3, 8185],
+                         chunk=4096, keep_percent=25, config_id=230, steps=2)
+    assert wl.N % 8 == 0
+    sep = GpuRun(wl, "pipeline")
+    buck = GpuRun(wl, "pipeline")
+    st = oracle.State(workload.initial_weights(wl))
+    for s in range(2):
+        g_np = workload.all_grads(wl, s)
+        bucket = torch.empty(wl.W * wl.N, dtype=torch.float16, device="cuda")
+        views, pos = [], 0
+        for w in range(wl.W):
+            row = []
+            for g in g_np[w]:
+                v = bucket[pos:pos + g.size]
+                v.copy_(torch.from_numpy(g))
+                row.append(v)
+                pos += g.size
+            views.append(row)
+        sep.step(dev_grads(g_np))
+        buck.step(views)
+        a, b = sep.snapshot(), buck.snapshot()
+        _compare_paths(a, b)
+        oracle_step(g_np, st, wl, b)
