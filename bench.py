@@ -228,12 +228,18 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def phase1_kernel(wl) -> str:
-    """Which kernel phase 1 uses for this layout (mirrors the library's
-    choice: TMA staging for 4, 8 or 16 workers when every layer starts at a
-    multiple of 8 elements and the chunk is a multiple of 256)."""
-    aligned = all(s % 8 == 0 for s in wl.sizes) and wl.chunk % 256 == 0
-    return "k_reduce_tma" if wl.W in (4, 8, 16) and aligned else "k_reduce"
+def phase1_kernel(wl, table=None) -> str:
+    """The phase-1 kernel the library picks for this layout
+    (fc_step_reduce_kernel).  Without a table of the gradients actually
+    used, separately allocated 512-byte-aligned tensors are assumed."""
+    from gradient_aggregation_gb300 import fc
+    if table is None:
+        table = fc.PtrTable.from_addresses(
+            [[(1 + w * wl.L + l) << 20 for l in range(wl.L)] for w in range(wl.W)], wl.sizes)
+    kind = fc.fc_step_reduce_kernel(table, wl.chunk)
+    return {fc.FC_REDUCE_REGISTER: "k_reduce",
+            fc.FC_REDUCE_STAGED: "k_reduce_tma",
+            fc.FC_REDUCE_STAGED_SHIFTED: "k_reduce_tma, shifted layout"}[kind]
 
 
 def traffic_from_profile(src_hash, wl):
@@ -483,7 +489,7 @@ def run_gpu(args, wl, rank, world, local):
                       % (step_bytes / 1e9, 12 * N / 1e9)}),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "kernel": "phase 1 of fc_step (%s)" % phase1_kernel(wl),
+                         "traffic": traffic, "kernel": "phase 1 of fc_step (%s)" % phase1_kernel(wl, table),
                          "algorithmic_bytes_per_launch": k_alg,
                          "avg_launch_ms": round(k_ms, 5), "peak_source": peak_src + " hbm_gbs",
                          "timed_launches": len(reduce_ms)},

@@ -161,21 +161,22 @@ fc_status check_f32(const void *p, const char *name, bool may_be_null)
 }
 
 // The TMA-staged phase 1 serves the tree order for 4, 8 or 16 workers, when
-// the layout keeps every bulk copy 16-byte aligned.
+// every layer has one address shift for all workers.  Returns the layout
+// (tma_layout) or 0 for the register kernel.
 template <class Tab>
-bool use_tma(const Tab &tab, const UnitGeom &G, const float *partials, int order)
+int use_tma(const Tab &tab, const UnitGeom &G, const float *partials, int order)
 {
 #ifdef FC_DISABLE_TMA
     (void)tab; (void)G; (void)partials; (void)order;
-    return false;
+    return 0;
 #else
     // With more than 16 workers a 64 KB stage holds fewer than eight units,
     // which leaves consumer warps idle; the register kernel streams those
     // layouts at the copy rate already.
     const int W = tab.W;
-    if (order != FC_ORDER_TREE) return false;
-    if (W != 4 && W != 8 && W != 16) return false;
-    return tma_eligible(tab, G, partials);
+    if (order != FC_ORDER_TREE) return 0;
+    if (W != 4 && W != 8 && W != 16) return 0;
+    return tma_layout(tab, G, partials);
 #endif
 }
 
@@ -447,20 +448,51 @@ fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
     if (fits_small(W, L)) {
         TableS tab;
         fill_table(tab, grads, W, L, sizes);
-        if (use_tma(tab, G, partials, order))
-            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream);
+        if (const int lay = use_tma(tab, G, partials, order))
+            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream, lay);
         else
             e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
     } else {
         static thread_local TableL tab;
         fill_table(tab, grads, W, L, sizes);
-        if (use_tma(tab, G, partials, order))
-            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream);
+        if (const int lay = use_tma(tab, G, partials, order))
+            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream, lay);
         else
             e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
     }
     if (e != cudaSuccess) return cuda_fail(e, "step_reduce launch");
     return ok();
+}
+
+int32_t fc_step_reduce_kernel(const void *const *grads, int32_t W, int32_t L,
+                              const int64_t *sizes, int64_t chunk, int32_t order)
+{
+    if (order < FC_ORDER_TREE || order > FC_ORDER_RING) {
+        fail(FC_ERR_INVALID_ARG, "order = %d is not an FC_ORDER_* value", order);
+        return -1;
+    }
+    int64_t N = 0;
+    if (check_sizes(L, sizes, &N) != FC_OK || check_table(grads, W, L, sizes) != FC_OK)
+        return -1;
+    if (chunk < 1) {
+        fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
+        return -1;
+    }
+    const UnitGeom G = ugeom(N, chunk);
+    // phase 1 always writes unit sums in the pipeline: any non-null marker
+    const float *partials = reinterpret_cast<const float *>(sizeof(float));
+    int lay;
+    if (fits_small(W, L)) {
+        TableS tab;
+        fill_table(tab, grads, W, L, sizes);
+        lay = use_tma(tab, G, partials, order);
+    } else {
+        static thread_local TableL tab;
+        fill_table(tab, grads, W, L, sizes);
+        lay = use_tma(tab, G, partials, order);
+    }
+    ok();
+    return lay == 1 ? FC_REDUCE_STAGED : lay == 2 ? FC_REDUCE_STAGED_SHIFTED : FC_REDUCE_REGISTER;
 }
 
 fc_status fc_step_reduce(const void *const *grads, int32_t W, int32_t L,

@@ -21,14 +21,16 @@ cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
                           const float *resid, float *out, float *partials,
                           cudaStream_t s, int order = 0);
 
-// TMA-staged phase 1 (tree order only).  tma_eligible: the layout and W
-// allow it; err: a device word set if a wait inside the kernel gave up.
+// TMA-staged phase 1 (tree order only).  tma_layout: 0 if the layout does
+// not allow it, 1 for the aligned layout, 2 for the shifted one (layers at
+// any offset, one address shift per layer for all workers).  err: a device
+// word set if a wait inside the kernel gave up.
 template <class Tab>
-bool tma_eligible(const Tab &tab, const UnitGeom &G, const float *partials);
+int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials);
 template <class Tab>
 cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
                               const float *resid, float *out, float *partials,
-                              unsigned *err, cudaStream_t s);
+                              unsigned *err, cudaStream_t s, int layout);
 
 template <class Tab>
 cudaError_t launch_pack(const Tab &tab, int64_t N, __half *fused,

@@ -1,7 +1,5 @@
 // Phase 1 (a2 + unit sums of squares) with TMA staging, for 4, 8 or 16
-// workers and layouts where every layer is 16-byte aligned for every worker
-// and starts at a multiple of 8 elements, N is a multiple of 8 and the chunk
-// size a multiple of 256.
+// workers, N a multiple of 8 and a chunk size that is a multiple of 256.
 //
 // One CTA per SM: a producer warp streams tiles of TT fused elements of all
 // W workers (and the residual) from HBM into a ring of S shared-memory stages
@@ -11,6 +9,24 @@
 // and write `a` and the unit sums of squares exactly as k_reduce does, so the
 // results are bit-identical.  The copies keep S-1 tiles of every worker in
 // flight per SM regardless of register pressure.
+//
+// Two layouts:
+//  * aligned (MIS = false): every layer starts at a multiple of 8 fused
+//    elements and every worker's copy of it is 16-byte aligned there.  Each
+//    worker row of a stage holds the tile's TT elements in fused order.
+//  * shifted (MIS = true): layers may start anywhere, as long as each layer's
+//    address, taken modulo 16 bytes at a given fused index, is the same for
+//    every worker (true for separately allocated tensors and for buckets).
+//    A bulk copy must start and end on 16-byte boundaries, so each layer
+//    piece of a tile lands in shared memory at the same position modulo 16
+//    bytes as in global memory: element u of the tile sits at u + sh, sh =
+//    the layer's shift (0..7 elements) plus a gap (a multiple of 8) that
+//    keeps the pieces apart.  The producer copies the 16-byte-aligned part
+//    of every piece (running past the tile's ends where the layer goes on)
+//    and records the pieces in a small table in the stage.  A consumer reads
+//    its 8 elements with two 16-byte shared-memory loads and a funnel shift;
+//    only groups not fully inside one copied piece (at layer boundaries)
+//    read their elements from global memory.
 //
 // Every wait on an mbarrier gives up after a time limit (read from the
 // global timer); the kernel then records the failure in `err` and returns,
@@ -94,11 +110,44 @@ constexpr int kConsumerWarps = 8;
 constexpr int kThreads = 32 * (kConsumerWarps + 1);
 constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any tile
 
+// Shifted layout: extra elements per worker row (room for the shifts and
+// gaps of the pieces), and entries of a stage's piece table.  A tile whose
+// pieces need more room, or more entries, leaves the rest unstaged (read
+// from global memory by the consumers).
+constexpr int kSlack = 64;
+constexpr int kMaxPieces = 32;
+
+__device__ __forceinline__ int64_t round_down8(int64_t x) { return x & ~(int64_t)7; }
+__device__ __forceinline__ int64_t round_up8(int64_t x) { return (x + 7) & ~(int64_t)7; }
+
+// Shift, in elements (0..7), of layer l: its worker-0 address at fused
+// index 0 modulo 16 bytes, halved.
+template <class Tab>
+__device__ __forceinline__ int layer_shift(const Tab &tab, int l)
+{
+    return (int)((((uintptr_t)tab.ptr[l]) - 2u * (uintptr_t)tab.off[l]) >> 1) & 7;
+}
+
+// 8 fp16 values starting `d` halves (0..7) into the 16 halves a:b.
+__device__ __forceinline__ uint4 funnel8(const uint4 &a, const uint4 &b, int d)
+{
+    uint32_t w0 = a.x, w1 = a.y, w2 = a.z, w3 = a.w, w4 = b.x, w5 = b.y, w6 = b.z, w7 = b.w;
+    if (d & 4) { w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7; }
+    if (d & 2) { w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5; }
+    if (d & 1) {
+        w0 = __funnelshift_r(w0, w1, 16);
+        w1 = __funnelshift_r(w1, w2, 16);
+        w2 = __funnelshift_r(w2, w3, 16);
+        w3 = __funnelshift_r(w3, w4, 16);
+    }
+    return make_uint4(w0, w1, w2, w3);
+}
+
 }  // namespace
 
 // drop_tile >= 0 (test hook only, see fc_test_stage_loss): the producer
 // issues no copies for that tile, so the bounded waits on it run out.
-template <class Tab, int WT, int MAXH>
+template <class Tab, int WT, int MAXH, bool MIS>
 __global__ void __launch_bounds__(kThreads, 1)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
@@ -110,8 +159,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned char *stages = smem + 128;
     const int W = WT > 0 ? WT : tab.W;
     const int L = tab.L;
-    const size_t gbytes = (size_t)W * TT * 2;
-    const size_t sbytes = gbytes + (size_t)TT * 4;
+    const int ROW = TT + (MIS ? kSlack : 0);  // elements per worker row
+    const size_t gbytes = (size_t)W * ROW * 2;
+    const size_t sbytes = gbytes + (size_t)TT * 4 + (MIS ? kMaxPieces * sizeof(int4) : 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t N = G.N;
     const int64_t ntiles = (N + TT - 1) / TT;
@@ -143,18 +193,71 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int64_t f0 = t * TT;
             const int64_t f1 = f0 + TT < N ? f0 + TT : N;
             const uint32_t full = smem_u32(&bars[s]);
-            mbar_expect_tx(full, (uint32_t)((f1 - f0) * (2 * W + (resid ? 4 : 0))));
             unsigned char *st = stages + (size_t)s * sbytes;
-            int l = find_layer(tab, f0);
-            for (int64_t fa = f0; fa < f1;) {
-                while (tab.off[l + 1] <= fa) ++l;
-                const int64_t fb = tab.off[l + 1] < f1 ? tab.off[l + 1] : f1;
-                for (int w = 0; w < W; ++w)
-                    bulk_g2s(smem_u32(st + ((size_t)w * TT + (size_t)(fa - f0)) * 2),
-                             tab.ptr[w * L + l] + (fa - tab.off[l]), (uint32_t)((fb - fa) * 2), full);
-                fa = fb;
+            const uint32_t rbytes = resid ? (uint32_t)((f1 - f0) * 4) : 0u;
+            if constexpr (!MIS) {
+                mbar_expect_tx(full, (uint32_t)((f1 - f0) * 2 * W) + rbytes);
+                int l = find_layer(tab, f0);
+                for (int64_t fa = f0; fa < f1;) {
+                    while (tab.off[l + 1] <= fa) ++l;
+                    const int64_t fb = tab.off[l + 1] < f1 ? tab.off[l + 1] : f1;
+                    for (int w = 0; w < W; ++w)
+                        bulk_g2s(smem_u32(st + ((size_t)w * ROW + (size_t)(fa - f0)) * 2),
+                                 tab.ptr[w * L + l] + (fa - tab.off[l]),
+                                 (uint32_t)((fb - fa) * 2), full);
+                    fa = fb;
+                }
+            } else {
+                // Piece table: {end of the piece (tile-relative), sh (or -1
+                // if unstaged), layer, copied range [lo, hi) of the row as
+                // lo | hi << 16}.  The last entry always ends at the tile's end.
+                int4 *pieces = reinterpret_cast<int4 *>(st + gbytes + (size_t)TT * 4);
+                int n = 0, gap = 0, prev_d = -1;
+                uint32_t row_bytes = 0;
+                int l = find_layer(tab, f0);
+                for (int64_t fa = f0; fa < f1;) {
+                    while (tab.off[l + 1] <= fa) ++l;
+                    const int64_t fb = tab.off[l + 1] < f1 ? tab.off[l + 1] : f1;
+                    if (n == kMaxPieces - 1) {
+                        pieces[n++] = make_int4((int)(f1 - f0), -1, l, 0);
+                        break;
+                    }
+                    const int d = layer_shift(tab, l);
+                    const int g = gap + (prev_d > d ? 8 : 0);
+                    const int64_t sh = g + d;
+                    // copied row range: the 16-byte frames around the piece,
+                    // clipped to the layer's own elements
+                    int64_t plo = round_down8(fa - f0 + sh);
+                    const int64_t lay_lo = tab.off[l] - f0 + sh;
+                    if (plo < lay_lo) plo = round_up8(lay_lo);
+                    int64_t phi = round_up8(fb - f0 + sh);
+                    const int64_t lay_hi = tab.off[l + 1] - f0 + sh;
+                    if (phi > lay_hi) phi = round_down8(lay_hi);
+                    if (phi > ROW) {
+                        pieces[n++] = make_int4((int)(fb - f0), -1, l, 0);
+                    } else {
+                        if (phi < plo) phi = plo;
+                        pieces[n++] = make_int4((int)(fb - f0), (int)sh, l,
+                                                (int)(plo | (phi << 16)));
+                        row_bytes += (uint32_t)(phi - plo) * 2;
+                        gap = g;
+                        prev_d = d;
+                    }
+                    fa = fb;
+                }
+                // the arrive (release) also publishes the piece table
+                mbar_expect_tx(full, row_bytes * (uint32_t)W + rbytes);
+                for (int i = 0; i < n; ++i) {
+                    const int4 pc = pieces[i];
+                    const int plo = pc.w & 0xffff, phi = pc.w >> 16;
+                    if (pc.y < 0 || phi <= plo) continue;
+                    const int64_t j = f0 + plo - pc.y - tab.off[pc.z];  // layer element at row plo
+                    for (int w = 0; w < W; ++w)
+                        bulk_g2s(smem_u32(st + ((size_t)w * ROW + (size_t)plo) * 2),
+                                 tab.ptr[w * L + pc.z] + j, (uint32_t)(phi - plo) * 2, full);
+                }
             }
-            if (resid) bulk_g2s(smem_u32(st + gbytes), resid + f0, (uint32_t)((f1 - f0) * 4), full);
+            if (resid) bulk_g2s(smem_u32(st + gbytes), resid + f0, rbytes, full);
         }
         // No copy may still be landing in shared memory when the CTA exits:
         // wait for every stage still in flight (each wait bounded; a stage
@@ -184,12 +287,51 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (f < hi) {  // f + 8 <= hi: N and every unit start are multiples of 8
                 const size_t off = (size_t)(f - f0);
                 float a[8];
-                tree_sum<WT, MAXH, 8>(
-                    W,
-                    [&](int w, float(&x)[8]) {
-                        unpack8(*reinterpret_cast<const uint4 *>(st + ((size_t)w * TT + off) * 2), x);
-                    },
-                    a);
+                if constexpr (!MIS) {
+                    tree_sum<WT, MAXH, 8>(
+                        W,
+                        [&](int w, float(&x)[8]) {
+                            unpack8(*reinterpret_cast<const uint4 *>(st + ((size_t)w * ROW + off) * 2), x);
+                        },
+                        a);
+                } else {
+                    const int uu = (int)off;
+                    const int4 *pieces = reinterpret_cast<const int4 *>(st + gbytes + (size_t)TT * 4);
+                    int4 pc = pieces[0];
+                    for (int i = 1; pc.x <= uu; ++i) pc = pieces[i];
+                    const int plo = pc.w & 0xffff, phi = pc.w >> 16;
+                    if (pc.y >= 0 && uu + 8 <= pc.x && uu + pc.y >= plo && uu + pc.y + 8 <= phi) {
+                        // all 8 in one copied piece: two aligned loads, shifted
+                        const int p0 = uu + (pc.y & ~7), d = pc.y & 7;
+                        tree_sum<WT, MAXH, 8>(
+                            W,
+                            [&](int w, float(&x)[8]) {
+                                const uint4 *q = reinterpret_cast<const uint4 *>(
+                                    st + ((size_t)w * ROW + p0) * 2);
+                                const uint4 qa = q[0];
+                                unpack8(d ? funnel8(qa, q[1], d) : qa, x);
+                            },
+                            a);
+                    } else {
+                        // at a layer boundary (or unstaged): from global memory
+                        int l = pc.z, lay[8];
+                        int64_t jj[8];
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            while (tab.off[l + 1] <= f + e) ++l;
+                            lay[e] = l;
+                            jj[e] = f + e - tab.off[l];
+                        }
+                        tree_sum<WT, MAXH, 8>(
+                            W,
+                            [&](int w, float(&x)[8]) {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e)
+                                    x[e] = ld_half_as_float(tab.ptr[w * L + lay[e]] + jj[e]);
+                            },
+                            a);
+                    }
+                }
                 float r[8];
                 if (resid) {
                     const float4 *rr = reinterpret_cast<const float4 *>(st + gbytes + off * 4);
@@ -216,13 +358,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Tile size and stage count for W workers: a stage holds W*TT fp16 values and
-// TT fp32 residuals, about 64 KB of gradients, and as many stages as fit.
-static void tma_shape(int W, int &TT, int &S, size_t &smem)
+// Tile size and stage count for W workers: a stage holds W rows of TT fp16
+// values (plus the slack of the shifted layout), TT fp32 residuals and the
+// piece table; about 64 KB of gradients, and as many stages as fit.
+static void tma_shape(int W, bool mis, int &TT, int &S, size_t &smem)
 {
     TT = 2048;
     while (TT > FC_UNIT && (size_t)W * TT * 2 > 65536) TT /= 2;
-    const size_t sbytes = (size_t)W * TT * 2 + (size_t)TT * 4;
+    const size_t row = (size_t)TT + (mis ? kSlack : 0);
+    const size_t sbytes = (size_t)W * row * 2 + (size_t)TT * 4 +
+                          (mis ? kMaxPieces * sizeof(int4) : 0);
     const size_t cap = 227 * 1024 - 128;
     S = (int)(cap / sbytes);
     if (S > 4) S = 4;
@@ -230,29 +375,35 @@ static void tma_shape(int W, int &TT, int &S, size_t &smem)
 }
 
 template <class Tab>
-bool tma_eligible(const Tab &tab, const UnitGeom &G, const float *partials)
+int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
 {
-    if (partials && G.cs % FC_UNIT != 0) return false;
-    if (G.N % 8 != 0) return false;
+    if (partials && G.cs % FC_UNIT != 0) return 0;
+    if (G.N % 8 != 0) return 0;
+    bool aligned = true;
     for (int l = 0; l < tab.L; ++l) {
-        if (tab.off[l] % 8 != 0) return false;
-        if (tab.off[l + 1] > tab.off[l] && !((tab.vec[l >> 5] >> (l & 31)) & 1u)) return false;
+        if (tab.off[l] % 8 != 0 || !((tab.vec[l >> 5] >> (l & 31)) & 1u)) aligned = false;
+        // the shifted layout needs one shift per layer, the same for all workers
+        const uintptr_t s0 = ((uintptr_t)tab.ptr[l] - 2u * (uintptr_t)tab.off[l]) & 15u;
+        for (int w = 1; w < tab.W; ++w)
+            if ((((uintptr_t)tab.ptr[w * tab.L + l] - 2u * (uintptr_t)tab.off[l]) & 15u) != s0)
+                return 0;
     }
     int TT, S;
     size_t smem;
-    tma_shape(tab.W, TT, S, smem);
-    return S >= 2;
+    tma_shape(tab.W, !aligned, TT, S, smem);
+    if (S < 2) return 0;
+    return aligned ? 1 : 2;
 }
 
-template <class Tab, int WT, int MAXH>
+template <class Tab, int WT, int MAXH, bool MIS>
 static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                                 const float *resid, float *out, float *partials,
                                 unsigned *err, cudaStream_t s)
 {
     int TT, S;
     size_t smem;
-    tma_shape(tab.W, TT, S, smem);
-    auto kern = k_reduce_tma<Tab, WT, MAXH>;
+    tma_shape(tab.W, MIS, TT, S, smem);
+    auto kern = k_reduce_tma<Tab, WT, MAXH, MIS>;
     static std::mutex mu;
     static bool attr_set[64];
     int dev = 0;
@@ -275,17 +426,29 @@ static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                               resid, out, partials, err, drop, limit);
 }
 
+template <class Tab, bool MIS>
+static cudaError_t launch_tma_layout(const Tab &tab, const UnitGeom &G, float u,
+                                     const float *resid, float *out, float *partials,
+                                     unsigned *err, cudaStream_t s)
+{
+    switch (tab.W) {
+    case 4: return launch_tma_w<Tab, 4, 3, MIS>(tab, G, u, resid, out, partials, err, s);
+    case 8: return launch_tma_w<Tab, 8, 4, MIS>(tab, G, u, resid, out, partials, err, s);
+    case 16: return launch_tma_w<Tab, 16, 5, MIS>(tab, G, u, resid, out, partials, err, s);
+    default: break;
+    }
+    return cudaErrorNotSupported;
+}
+
 template <class Tab>
 cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
                               const float *resid, float *out, float *partials,
-                              unsigned *err, cudaStream_t s)
+                              unsigned *err, cudaStream_t s, int layout)
 {
-    switch (tab.W) {
-    case 4: return launch_tma_w<Tab, 4, 3>(tab, G, u, resid, out, partials, err, s);
-    case 8: return launch_tma_w<Tab, 8, 4>(tab, G, u, resid, out, partials, err, s);
-    case 16: return launch_tma_w<Tab, 16, 5>(tab, G, u, resid, out, partials, err, s);
-    default: break;
-    }
+    if (layout == 1)
+        return launch_tma_layout<Tab, false>(tab, G, u, resid, out, partials, err, s);
+    if (layout == 2)
+        return launch_tma_layout<Tab, true>(tab, G, u, resid, out, partials, err, s);
     return cudaErrorNotSupported;
 }
 
@@ -302,13 +465,13 @@ extern "C" fc_status fc_test_stage_loss(int64_t tile, uint64_t wait_limit_ns)
 
 namespace fc {
 
-template bool tma_eligible<TableS>(const TableS &, const UnitGeom &, const float *);
-template bool tma_eligible<TableL>(const TableL &, const UnitGeom &, const float *);
+template int tma_layout<TableS>(const TableS &, const UnitGeom &, const float *);
+template int tma_layout<TableL>(const TableL &, const UnitGeom &, const float *);
 template cudaError_t launch_reduce_tma<TableS>(const TableS &, const UnitGeom &, float,
                                                const float *, float *, float *,
-                                               unsigned *, cudaStream_t);
+                                               unsigned *, cudaStream_t, int);
 template cudaError_t launch_reduce_tma<TableL>(const TableL &, const UnitGeom &, float,
                                                const float *, float *, float *,
-                                               unsigned *, cudaStream_t);
+                                               unsigned *, cudaStream_t, int);
 
 }  // namespace fc

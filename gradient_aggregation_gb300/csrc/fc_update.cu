@@ -31,7 +31,13 @@ __device__ __forceinline__ void sgd1(float a, bool kept, float lr, float mu,
     w = __fsub_rn(w, v);
 }
 
-__global__ void __launch_bounds__(FC_BLOCK)
+// Threads per block of the update (each tile of 2048 elements is 512
+// 16-byte groups, spread over the block's threads).
+#ifndef FC_UPDATE_BLOCK
+#define FC_UPDATE_BLOCK 128
+#endif
+
+__global__ void __launch_bounds__(FC_UPDATE_BLOCK)
     k_update(const TileGeom G, const int64_t tiles, const float *a,
              const uint8_t *__restrict__ mask, const int32_t *__restrict__ slot,
              float *__restrict__ packed, __half *__restrict__ packed16,
@@ -56,7 +62,8 @@ __global__ void __launch_bounds__(FC_BLOCK)
         const int64_t pbase = pk ? (int64_t)sl * cs - c * cs : 0;
         if (any) {
             const int64_t q1 = (hi + 3) >> 2;
-            for (int64_t q = (lo >> 2) + threadIdx.x; q < q1; q += FC_BLOCK) {
+#pragma unroll 4
+            for (int64_t q = (lo >> 2) + threadIdx.x; q < q1; q += FC_UPDATE_BLOCK) {
                 const int64_t i0 = q << 2;
                 if (i0 >= lo && i0 + 4 <= hi) {
                     float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
@@ -127,7 +134,7 @@ __global__ void __launch_bounds__(FC_BLOCK)
         // zero the packed slot beyond N (short last chunk)
         if (pk && hin > hi) {
             const int64_t p0 = lo > G.N ? lo : G.N;
-            for (int64_t i = p0 + threadIdx.x; i < hin; i += FC_BLOCK) {
+            for (int64_t i = p0 + threadIdx.x; i < hin; i += FC_UPDATE_BLOCK) {
                 if (packed) packed[pbase + i] = 0.f;
                 if (packed16) packed16[pbase + i] = __float2half_rn(0.f);
             }
@@ -141,8 +148,8 @@ cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           float lr, float mu, float *r, float *v, float *w,
                           __half *w16, bool inplace, cudaStream_t s)
 {
-    const int grid = grid_for((const void *)k_update, FC_BLOCK, 0, tiles);
-    return launch_after_prior(k_update, (unsigned)grid, FC_BLOCK, 0, s, G, tiles,
+    const int grid = grid_for((const void *)k_update, FC_UPDATE_BLOCK, 0, tiles);
+    return launch_after_prior(k_update, (unsigned)grid, FC_UPDATE_BLOCK, 0, s, G, tiles,
                               a, mask, slot, packed, packed16, send_scale, lr,
                               mu, r, v, w, w16, inplace ? 1 : 0);
 }

@@ -29,6 +29,7 @@ FC_MAX_TABLE_PTRS = 3072
 FC_MAX_TABLE_LAYERS = 512
 FC_NOALLOC_WORKSPACE_BYTES = 4 << 20
 FC_ORDER_TREE, FC_ORDER_SEQUENTIAL, FC_ORDER_RING = 0, 1, 2
+FC_REDUCE_REGISTER, FC_REDUCE_STAGED, FC_REDUCE_STAGED_SHIFTED = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -46,6 +47,7 @@ _SIGS = {
     "fc_reduce_ordered": (ctypes.c_int, [_P, _I32, _I64, _F32, _P, _P, _I32, _P]),
     "fc_step_reduce_ordered": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _I32,
                                               _P, _SZ, _P]),
+    "fc_step_reduce_kernel": (_I32, [_P, _I32, _I32, _P, _I64, _I32]),
     "fc_chunk_norms": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "fc_chunk_select": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _P, _F32,
                                        _P, _P]),
@@ -129,6 +131,20 @@ class PtrTable:
             *[grads[w][l].data_ptr() for w in range(self.W) for l in range(self.L)])
         self._sizes = _i64(sizes)
         self._keep = grads  # keep the tensors alive while the table is used
+
+    @classmethod
+    def from_addresses(cls, addresses: List[List[int]], sizes: Sequence[int]) -> "PtrTable":
+        """A table of plain device addresses ([worker][layer]), for calls
+        that only inspect the layout (fc_step_reduce_kernel)."""
+        t = cls.__new__(cls)
+        t.W, t.L = len(addresses), len(sizes)
+        t.sizes = [int(x) for x in sizes]
+        t.N = sum(t.sizes)
+        t._ptrs = (ctypes.c_void_p * (t.W * t.L))(
+            *[int(addresses[w][l]) for w in range(t.W) for l in range(t.L)])
+        t._sizes = _i64(t.sizes)
+        t._keep = None
+        return t
 
     @property
     def ptrs(self):
@@ -243,6 +259,17 @@ def fc_step_reduce_ordered(grads, loss_scale: float, chunk: int,
     _check(lib().fc_step_reduce_ordered(t.ptrs, t.W, t.L, t.sizes_c, float(loss_scale),
                                         int(chunk), _p(residual), _p(a), int(order),
                                         _p(workspace), workspace.numel(), _s(stream)))
+
+
+def fc_step_reduce_kernel(grads, chunk: int, order: int = FC_ORDER_TREE) -> int:
+    """FC_REDUCE_* of the phase-1 kernel the library picks for this layout
+    (host only; `grads` is [worker][layer] tensors or a PtrTable, which
+    PtrTable.from_addresses can build from plain addresses)."""
+    t = _table(grads)
+    r = int(lib().fc_step_reduce_kernel(t.ptrs, t.W, t.L, t.sizes_c, int(chunk), int(order)))
+    if r < 0:
+        _check(FC_ERR_INVALID_ARG)
+    return r
 
 
 def fc_step_select(N: int, chunk: int, k: int, norms: torch.Tensor, idx: torch.Tensor,

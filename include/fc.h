@@ -251,6 +251,26 @@ FC_API fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
                                         int32_t order, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
+/* Which phase-1 kernel fc_step_reduce_ordered (and so fc_step) launches for
+ * this layout of gradients (arguments as there; chunk > 0, order an
+ * FC_ORDER_* value).  Host only: the pointers are compared, never read, and
+ * no device work is done.  Returns FC_REDUCE_* below, or -1 (message in
+ * fc_last_error) for arguments the reduction would reject.  The kernels
+ * produce the same bits; the choice only changes speed.
+ *  FC_REDUCE_REGISTER        register streaming, one warp per 256-element unit;
+ *  FC_REDUCE_STAGED          bulk copies staged in shared memory, every layer
+ *                            at a multiple of 8 elements and 16-byte aligned
+ *                            for every worker (4, 8 or 16 workers);
+ *  FC_REDUCE_STAGED_SHIFTED  the same for layers at any offset whose address
+ *                            modulo 16 bytes, at a given fused index, is the
+ *                            same for every worker. */
+#define FC_REDUCE_REGISTER 0
+#define FC_REDUCE_STAGED 1
+#define FC_REDUCE_STAGED_SHIFTED 2
+FC_API int32_t fc_step_reduce_kernel(const void *const *grads, int32_t W,
+                                     int32_t L, const int64_t *sizes,
+                                     int64_t chunk, int32_t order);
+
 /* Phase 2: finishes the chunk norms from phase 1's unit sums (norms [C],
  * device output, bitwise the same as fc_chunk_norms on a) and selects the
  * top k chunks exactly as fc_chunk_select does (idx [k], mask [C],

@@ -129,3 +129,43 @@ def test_python_binding_raises_with_message(fc_lib):
     with pytest.raises(fc.FcError) as e:
         fc._check(fc_lib.fc_tree_reduce(0x10000, 0, 10, 1.0, None, 0x10000, None))
     assert e.value.status == fc.FC_ERR_INVALID_ARG and "W = 0" in str(e.value)
+
+
+def test_reduce_kernel_choice_from_layout(fc_lib):
+    """fc_step_reduce_kernel inspects addresses only: fake ones will do."""
+    from gradient_aggregation_gb300 import fc
+    T = fc.PtrTable.from_addresses
+
+    def separate(W, sizes, skew=lambda w, l: 0):
+        return T([[((1 + w * len(sizes) + l) << 20) + skew(w, l) for l in range(len(sizes))]
+                  for w in range(W)], sizes)
+
+    def bucket(W, sizes):
+        off, n = fc.fc_layout(sizes)
+        return T([[((1 + w) << 32) + 2 * o for o in off] for w in range(W)], sizes)
+
+    even, odd = [4096, 800, 8], [1001, 64, 3333, 2]       # N = 4904, 4400
+    k = fc.fc_step_reduce_kernel
+    assert k(separate(16, even), 256) == fc.FC_REDUCE_STAGED
+    assert k(separate(8, odd), 512) == fc.FC_REDUCE_STAGED_SHIFTED
+    assert k(separate(4, odd), 256) == fc.FC_REDUCE_STAGED_SHIFTED
+    # a bucket per worker is one aligned segment, whatever the layer sizes
+    assert k(bucket(16, odd), 256) == fc.FC_REDUCE_STAGED
+    # every worker 2 bytes past a 16-byte boundary: one shift for all
+    assert k(separate(16, even, lambda w, l: 2), 256) == fc.FC_REDUCE_STAGED_SHIFTED
+    # one worker shifted differently from the others: register kernel
+    assert k(separate(16, even, lambda w, l: 2 if (w, l) == (3, 1) else 0), 256) == \
+        fc.FC_REDUCE_REGISTER
+    # worker counts, orders, chunk sizes and N the staged kernel does not serve
+    assert k(separate(32, even), 256) == fc.FC_REDUCE_REGISTER
+    assert k(separate(2, even), 256) == fc.FC_REDUCE_REGISTER
+    assert k(separate(8, even), 256, fc.FC_ORDER_SEQUENTIAL) == fc.FC_REDUCE_REGISTER
+    assert k(separate(8, even), 256, fc.FC_ORDER_RING) == fc.FC_REDUCE_REGISTER
+    assert k(separate(8, even), 300) == fc.FC_REDUCE_REGISTER
+    assert k(separate(8, [1001, 64, 3333]), 256) == fc.FC_REDUCE_REGISTER   # N % 8 != 0
+    with pytest.raises(fc.FcError):
+        k(separate(8, even), 256, 7)
+    with pytest.raises(fc.FcError):
+        k(separate(8, even), 0)
+    with pytest.raises(fc.FcError):
+        k(separate(8, even, lambda w, l: 1), 256)                          # odd address

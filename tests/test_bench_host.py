@@ -70,7 +70,8 @@ def test_phase1_kernel_choice_and_profile_parsing():
     from gradient_aggregation_gb300 import workload
     assert bench.phase1_kernel(workload.get("alexnet")) == "k_reduce_tma"
     assert bench.phase1_kernel(workload.get("stress")) == "k_reduce"      # 64 workers
-    assert bench.phase1_kernel(workload.get("googlenet")) == "k_reduce"   # misaligned layers
+    # layers at odd offsets, one address shift per layer for all workers
+    assert bench.phase1_kernel(workload.get("googlenet")) == "k_reduce_tma, shifted layout"
     wl = workload.get("alexnet")
     # the committed summary is used only for the kernel source it was taken on
     assert bench.traffic_from_profile("not-the-current-source", wl) is None

@@ -31,7 +31,7 @@ def _compare_paths(p, s):
             assert bits_equal(np.asarray(p[key]), np.asarray(s[key])), key
 
 
-def _run_workload(wl, steps=None, both_paths=True):
+def _run_workload(wl, steps=None, both_paths=True, expect_kernel=None, to_dev=dev_grads):
     steps = wl.steps if steps is None else steps
     runs = [GpuRun(wl, "pipeline")]
     if both_paths:
@@ -40,7 +40,9 @@ def _run_workload(wl, steps=None, both_paths=True):
     reports = []
     for s in range(steps):
         g_np = workload.all_grads(wl, s)
-        g_dev = dev_grads(g_np)
+        g_dev = to_dev(g_np)
+        if expect_kernel is not None:
+            assert fc.fc_step_reduce_kernel(g_dev, wl.chunk) == expect_kernel
         snaps = []
         for r in runs:
             r.step(g_dev)
@@ -55,11 +57,82 @@ def _run_workload(wl, steps=None, both_paths=True):
     return reports
 
 
+WORKLOAD_KERNEL = {"tiny": fc.FC_REDUCE_STAGED, "nin": fc.FC_REDUCE_STAGED_SHIFTED,
+                   "googlenet": fc.FC_REDUCE_STAGED_SHIFTED, "alexnet": fc.FC_REDUCE_STAGED,
+                   "stress": fc.FC_REDUCE_REGISTER}
+
+
 @pytest.mark.parametrize("name", ["tiny", "nin", "googlenet", "alexnet", "stress"])
 def test_workload_parity(name):
     wl = workload.get(name)
-    reports = _run_workload(wl, both_paths=name != "stress")
+    reports = _run_workload(wl, both_paths=name != "stress",
+                            expect_kernel=WORKLOAD_KERNEL[name])
     assert len(reports) == wl.steps
+
+
+def _sizes_n8(sizes):
+    """Pads the last layer so that N is a multiple of 8 (the staged kernels'
+    condition)."""
+    sizes = [int(x) for x in sizes]
+    sizes[-1] += (-sum(sizes)) % 8
+    return sizes
+
+
+def _shifted_dev(shift_bytes):
+    """Device copies of every worker's layers starting `shift_bytes` past a
+    16-byte boundary (the same for all workers)."""
+    def to_dev(g_np):
+        out = []
+        for row in g_np:
+            r = []
+            for g in row:
+                buf = torch.empty(g.size + 8, dtype=torch.float16, device="cuda")
+                view = buf[shift_bytes // 2: shift_bytes // 2 + g.size]
+                view.copy_(torch.from_numpy(g))
+                assert view.data_ptr() % 16 == shift_bytes
+                r.append(view)
+            out.append(r)
+        return out
+    return to_dev
+
+
+def test_shifted_layout_odd_layer_sizes():
+    """Layers of odd sizes: every layer has its own shift, pieces start and
+    end inside tiles, the bulk copies run past the tile ends."""
+    rng = np.random.default_rng(7)
+    for W, chunk, cid in [(16, 512, 160), (8, 2048, 161), (4, 256, 162)]:
+        sizes = _sizes_n8(np.exp(rng.uniform(0, np.log(5000), 40)).astype(int) + 1)
+        wl = workload.custom(W=W, sizes=sizes, chunk=chunk, keep_percent=25,
+                             config_id=cid, steps=2, loss_scale=512.0)
+        _run_workload(wl, expect_kernel=fc.FC_REDUCE_STAGED_SHIFTED)
+
+
+def test_shifted_layout_many_tiny_layers():
+    """Hundreds of 1..20-element layers: tiles with more pieces than the
+    stage's piece table, whose rest is read from global memory."""
+    rng = np.random.default_rng(8)
+    sizes = _sizes_n8(rng.integers(1, 21, 300))
+    wl = workload.custom(W=8, sizes=sizes, chunk=256, keep_percent=30, config_id=163, steps=2)
+    _run_workload(wl, expect_kernel=fc.FC_REDUCE_STAGED_SHIFTED)
+
+
+def test_shifted_layout_gaps_past_the_slack():
+    """Runs of 9-element layers lower the shift at every boundary, so the gaps
+    between pieces outgrow the row's slack and later pieces are unstaged."""
+    sizes = _sizes_n8([9] * 20 + [5000] + [9] * 40 + [3000, 17, 2500])
+    for W, cid in [(4, 164), (16, 165)]:
+        wl = workload.custom(W=W, sizes=sizes, chunk=256, keep_percent=20, config_id=cid,
+                             steps=2)
+        _run_workload(wl, expect_kernel=fc.FC_REDUCE_STAGED_SHIFTED)
+
+
+@pytest.mark.parametrize("shift", [2, 6, 14])
+def test_shifted_layout_uniform_pointer_shift(shift):
+    """Layers at multiples of 8 elements, but every worker's tensors start
+    `shift` bytes past a 16-byte boundary."""
+    wl = workload.custom(W=16, sizes=[4096, 808, 8, 6000], chunk=256, keep_percent=25,
+                         config_id=166 + shift, steps=2)
+    _run_workload(wl, expect_kernel=fc.FC_REDUCE_STAGED_SHIFTED, to_dev=_shifted_dev(shift))
 
 
 SMALL_CASES = [
