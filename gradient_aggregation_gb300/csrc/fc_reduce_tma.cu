@@ -314,22 +314,20 @@ __global__ void __launch_bounds__(kThreads, 1)
                             a);
                     } else {
                         // at a layer boundary (or unstaged): from global memory
-                        int l = pc.z, lay[8];
-                        int64_t jj[8];
+                        int l = pc.z;
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             while (tab.off[l + 1] <= f + e) ++l;
-                            lay[e] = l;
-                            jj[e] = f + e - tab.off[l];
+                            const int64_t j = f + e - tab.off[l];
+                            float s1[1];
+                            tree_sum<WT, MAXH, 1>(
+                                W,
+                                [&](int w, float(&x)[1]) {
+                                    x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
+                                },
+                                s1);
+                            a[e] = s1[0];
                         }
-                        tree_sum<WT, MAXH, 8>(
-                            W,
-                            [&](int w, float(&x)[8]) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e)
-                                    x[e] = ld_half_as_float(tab.ptr[w * L + lay[e]] + jj[e]);
-                            },
-                            a);
                     }
                 }
                 float r[8];
