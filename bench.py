@@ -242,6 +242,20 @@ def phase1_kernel(wl, table=None) -> str:
             fc.FC_REDUCE_STAGED_SHIFTED: "k_reduce_tma, shifted layout"}[kind]
 
 
+def layer_groups_reverse(sizes, n_groups):
+    """Layer groups [first, end) in backprop order (last layer first), each
+    closed once it holds about 1/n_groups of the elements."""
+    total = sum(sizes)
+    groups, end, acc, target = [], len(sizes), 0, 1
+    for l in range(len(sizes) - 1, -1, -1):
+        acc += sizes[l]
+        if acc * n_groups >= total * target or l == 0:
+            groups.append((l, end))
+            end = l
+            target = acc * n_groups // total + 1   # a large layer may pass several marks
+    return groups
+
+
 def traffic_from_profile(src_hash, wl):
     """DRAM bytes per launch of the reduction kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -421,11 +435,38 @@ def run_gpu(args, wl, rank, world, local):
         bounds = [len(hv) * i // 4 for i in range(5)]
         parts = [(host[bounds[i]:bounds[i + 1]], stage[bounds[i]:bounds[i + 1]])
                  for i in range(4)]
+        # (d): backprop order, last layer first: each layer group's rows are
+        # copied in on their own stream, and phase 1 reduces the group's span
+        # as soon as its copy has landed (fc_step_reduce_span)
+        groups = layer_groups_reverse(wl.sizes, 4)
+        group_stream = torch.cuda.Stream(device=dev)
+        off_l, _ = fc.fc_layout(wl.sizes)
+        off_l = off_l + [N]
+        group_parts = [[(host[w * N + off_l[a]: w * N + off_l[b]],
+                         stage[w * N + off_l[a]: w * N + off_l[b]]) for w in range(W)]
+                       for a, b in groups]
         variants = {}
         for name, table, copy_in in (("copy_engine", fc.PtrTable(views(stage)), 1),
                                      ("copy_engine_x4", fc.PtrTable(views(stage)), 4),
+                                     ("layer_groups", fc.PtrTable(views(stage)), 2),
                                      ("zero_copy", fc.PtrTable(views(host)), 0)):
             def one_step():
+                if copy_in == 2:
+                    group_stream.wait_stream(s)     # the previous step is done with `stage`
+                    ready = []
+                    with torch.cuda.stream(group_stream):
+                        for part in group_parts:
+                            for hpart, dpart in part:
+                                dpart.copy_(hpart, non_blocking=True)
+                            ev = torch.cuda.Event()
+                            ev.record(group_stream)
+                            ready.append(ev)
+                    eng.step_layer_groups(table, groups, ready=ready, stream=s)
+                    with torch.cuda.stream(s):
+                        res_idx.copy_(eng.idx, non_blocking=True)
+                        res_thr.copy_(eng.threshold, non_blocking=True)
+                    s.synchronize()
+                    return int(res_idx[0]), float(res_thr[0])
                 if copy_in == 1:
                     with torch.cuda.stream(s):
                         stage.copy_(host, non_blocking=True)
@@ -465,6 +506,10 @@ def run_gpu(args, wl, rank, world, local):
                                        "gradients, then fc_step",
                         "copy_engine_x4": "the pinned-host -> device copy of all workers' "
                                           "gradients split over four streams, then fc_step",
+                        "layer_groups": "layer groups copied in last layer first on a copy "
+                                        "stream, phase 1 reducing each group's span as soon "
+                                        "as its copy lands (fc_step_reduce_span), then "
+                                        "select + update",
                         "zero_copy": "fc_step reading the pinned host gradients in place "
                                      "over the CPU-GPU link"}[best]
                        + "; kept indices + threshold copied back and read on the host",

@@ -419,14 +419,26 @@ static fc_status check_ws(int64_t N, int64_t chunk, void *ws, size_t bytes)
     return FC_OK;
 }
 
-fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
-                                 int32_t L, const int64_t *sizes,
-                                 float loss_scale, int64_t chunk,
-                                 const float *residual, float *a,
-                                 int32_t order, void *workspace,
-                                 size_t workspace_bytes, void *stream)
+// First unit (in the order of the unit index) whose first element is at or
+// after fused index f; G.units if none.
+static int64_t first_unit_at(const UnitGeom &G, int64_t f)
 {
-    TraceRange trace("fc_step_reduce_ordered");
+    if (f <= 0) return 0;
+    if (f >= G.N) return G.units;
+    const int64_t c = f / G.cs;
+    const int64_t j = ceil_div(f - c * G.cs, FC_UNIT);
+    const int64_t in_c = c + 1 < G.C ? G.U : G.units - c * G.U;
+    return j < in_c ? c * G.U + j : (c + 1) * G.U;
+}
+
+// Phase 1 over the units whose first element lies in [f_begin, f_end).
+static fc_status reduce_span(const char *name, const void *const *grads, int32_t W,
+                             int32_t L, const int64_t *sizes, float loss_scale,
+                             int64_t chunk, const float *residual, float *a, int32_t order,
+                             int64_t f_begin, int64_t f_end, bool whole, void *workspace,
+                             size_t workspace_bytes, void *stream)
+{
+    TraceRange trace(name);
     if (order < FC_ORDER_TREE || order > FC_ORDER_RING)
         return fail(FC_ERR_INVALID_ARG, "order = %d is not an FC_ORDER_* value", order);
     int64_t N = 0;
@@ -435,6 +447,13 @@ fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
     if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
     if (!(loss_scale > 0.f) || !isfinite(loss_scale))
         return fail(FC_ERR_INVALID_ARG, "loss_scale must be finite and > 0");
+    if (whole) {
+        f_begin = 0;
+        f_end = N;
+    } else if (f_begin < 0 || f_end < f_begin || f_end > N) {
+        return fail(FC_ERR_INVALID_ARG, "span [%lld, %lld) is not inside [0, N = %lld]",
+                    (long long)f_begin, (long long)f_end, (long long)N);
+    }
     TRY(check_f32(residual, "residual", true));
     TRY(check_f32(a, "a", false));
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
@@ -444,24 +463,61 @@ fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
     const WsLayout wl = ws_layout(N, chunk);
     float *partials = (float *)((char *)workspace + wl.partials);
     unsigned *err = (unsigned *)((char *)workspace + wl.counters) + 1;
+    const int64_t ub = first_unit_at(G, f_begin), ue = first_unit_at(G, f_end);
+    if (ub >= ue) return ok();
     cudaError_t e;
+    auto run = [&](const auto &tab) {
+        if (const int lay = use_tma(tab, G, partials, order)) {
+            // chunk % 256 == 0 here: unit j starts at 256 j
+            const int64_t fb = ub * FC_UNIT;
+            const int64_t fe = ue * FC_UNIT < N ? ue * FC_UNIT : N;
+            return launch_reduce_tma(tab, G, u, residual, a, partials, err,
+                                     (cudaStream_t)stream, lay, fb, fe);
+        }
+        return launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order,
+                             ub, ue);
+    };
     if (fits_small(W, L)) {
         TableS tab;
         fill_table(tab, grads, W, L, sizes);
-        if (const int lay = use_tma(tab, G, partials, order))
-            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream, lay);
-        else
-            e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
+        e = run(tab);
     } else {
         static thread_local TableL tab;
         fill_table(tab, grads, W, L, sizes);
-        if (const int lay = use_tma(tab, G, partials, order))
-            e = launch_reduce_tma(tab, G, u, residual, a, partials, err, (cudaStream_t)stream, lay);
-        else
-            e = launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order);
+        e = run(tab);
     }
     if (e != cudaSuccess) return cuda_fail(e, "step_reduce launch");
     return ok();
+}
+
+fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
+                                 int32_t L, const int64_t *sizes,
+                                 float loss_scale, int64_t chunk,
+                                 const float *residual, float *a,
+                                 int32_t order, void *workspace,
+                                 size_t workspace_bytes, void *stream)
+{
+    return reduce_span("fc_step_reduce_ordered", grads, W, L, sizes, loss_scale, chunk,
+                       residual, a, order, 0, 0, true, workspace, workspace_bytes, stream);
+}
+
+fc_status fc_step_reduce_span(const void *const *grads, int32_t W, int32_t L,
+                              const int64_t *sizes, float loss_scale, int64_t chunk,
+                              const float *residual, float *a, int64_t f_begin,
+                              int64_t f_end, void *workspace, size_t workspace_bytes,
+                              void *stream)
+{
+    return reduce_span("fc_step_reduce_span", grads, W, L, sizes, loss_scale, chunk, residual,
+                       a, FC_ORDER_TREE, f_begin, f_end, false, workspace, workspace_bytes,
+                       stream);
+}
+
+int64_t fc_unit_start(int64_t N, int64_t chunk, int64_t f)
+{
+    if (N < 1 || chunk < 1 || f < 0 || f > N) return -1;
+    if (f == N) return N;
+    const int64_t c = f / chunk;
+    return c * chunk + (f - c * chunk) / FC_UNIT * FC_UNIT;
 }
 
 int32_t fc_step_reduce_kernel(const void *const *grads, int32_t W, int32_t L,

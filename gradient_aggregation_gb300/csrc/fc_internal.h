@@ -14,12 +14,14 @@ template <class Tab>
 bool fill_table(Tab &t, const void *const *grads, int32_t W, int32_t L,
                 const int64_t *sizes);
 
-// Phase-1 / fc_tree_reduce kernel launch.  With partials != NULL the unit
-// sums of squares go to partials [G.units].  order: FC_ORDER_* of fc.h.
+// Phase-1 / fc_tree_reduce kernel launch over units [ub, ue) (ue < 0: all).
+// With partials != NULL the unit sums of squares go to partials [G.units].
+// order: FC_ORDER_* of fc.h.
 template <class Tab>
 cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
                           const float *resid, float *out, float *partials,
-                          cudaStream_t s, int order = 0);
+                          cudaStream_t s, int order = 0, int64_t ub = 0,
+                          int64_t ue = -1);
 
 // TMA-staged phase 1 (tree order only).  tma_layout: 0 if the layout does
 // not allow it, 1 for the aligned layout, 2 for the shifted one (layers at
@@ -27,10 +29,14 @@ cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
 // word set if a wait inside the kernel gave up.
 template <class Tab>
 int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials);
+// The staged kernel works on whole 256-element units: fused elements
+// [fb, fe) with fb a multiple of 256 and fe a multiple of 256 or N (fe < 0:
+// N).
 template <class Tab>
 cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
                               const float *resid, float *out, float *partials,
-                              unsigned *err, cudaStream_t s, int layout);
+                              unsigned *err, cudaStream_t s, int layout, int64_t fb = 0,
+                              int64_t fe = -1);
 
 template <class Tab>
 cudaError_t launch_pack(const Tab &tab, int64_t N, __half *fused,

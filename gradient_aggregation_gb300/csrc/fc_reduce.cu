@@ -35,7 +35,8 @@ template <class Tab, int WT, int MAXH, int ORDER>
 __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1
                                             : ((WT > 0 && WT <= 16) ? FC_REDUCE_MIN_BLOCKS_SMALL_W : 2))
     k_reduce(const __grid_constant__ Tab tab, const UnitGeom G, const float u,
-             const float *resid, float *out, float *partials)
+             const float *resid, float *out, float *partials, const int64_t u_begin,
+             const int64_t u_end)
 {
     const uint64_t pol = policy_evict_first();
     const int W = WT > 0 ? WT : tab.W;
@@ -47,8 +48,8 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1
     allow_dependent_launch();  // the selection may be scheduled; it waits for us
     const int64_t nwarps = ((int64_t)gridDim.x * blockDim.x) >> 5;
 
-    for (int64_t un = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-         un < G.units; un += nwarps) {
+    for (int64_t un = u_begin + (((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5);
+         un < u_end; un += nwarps) {
         int64_t c, lo, hi;
         unit_range(G, un, c, lo, hi);
         float tss = 0.f;
@@ -127,42 +128,50 @@ __global__ void __launch_bounds__(FC_BLOCK, (WT == 0 && MAXH > 7) ? 1
 template <class Tab, int WT, int MAXH, int ORDER = 0>
 static cudaError_t launch_reduce_w(const Tab &tab, const UnitGeom &G, float u,
                                    const float *resid, float *out,
-                                   float *partials, cudaStream_t s)
+                                   float *partials, cudaStream_t s, int64_t ub,
+                                   int64_t ue)
 {
     auto kern = k_reduce<Tab, WT, MAXH, ORDER>;
-    const int64_t blocks_needed = (G.units + FC_BLOCK / 32 - 1) / (FC_BLOCK / 32);
+    const int64_t blocks_needed = (ue - ub + FC_BLOCK / 32 - 1) / (FC_BLOCK / 32);
     const int grid = grid_for((const void *)kern, FC_BLOCK, 0, blocks_needed);
     return launch_after_prior(kern, (unsigned)grid, FC_BLOCK, 0, s, tab, G, u, resid,
-                              out, partials);
+                              out, partials, ub, ue);
 }
 
 template <class Tab>
 cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
                           const float *resid, float *out, float *partials,
-                          cudaStream_t s, int order)
+                          cudaStream_t s, int order, int64_t ub, int64_t ue)
 {
-    if (order == 1) return launch_reduce_w<Tab, 0, 1, 1>(tab, G, u, resid, out, partials, s);
-    if (order == 2) return launch_reduce_w<Tab, 0, 1, 2>(tab, G, u, resid, out, partials, s);
+    if (ue < 0) ue = G.units;
+    if (ub >= ue) return cudaSuccess;
+#define FC_R(WT, MAXH, ORDER) \
+    launch_reduce_w<Tab, WT, MAXH, ORDER>(tab, G, u, resid, out, partials, s, ub, ue)
+    if (order == 1) return FC_R(0, 1, 1);
+    if (order == 2) return FC_R(0, 1, 2);
     switch (tab.W) {
-    case 1: return launch_reduce_w<Tab, 1, 1>(tab, G, u, resid, out, partials, s);
-    case 2: return launch_reduce_w<Tab, 2, 2>(tab, G, u, resid, out, partials, s);
-    case 4: return launch_reduce_w<Tab, 4, 3>(tab, G, u, resid, out, partials, s);
-    case 8: return launch_reduce_w<Tab, 8, 4>(tab, G, u, resid, out, partials, s);
-    case 16: return launch_reduce_w<Tab, 16, 5>(tab, G, u, resid, out, partials, s);
-    case 32: return launch_reduce_w<Tab, 32, 6>(tab, G, u, resid, out, partials, s);
-    case 64: return launch_reduce_w<Tab, 64, 7>(tab, G, u, resid, out, partials, s);
+    case 1: return FC_R(1, 1, 0);
+    case 2: return FC_R(2, 2, 0);
+    case 4: return FC_R(4, 3, 0);
+    case 8: return FC_R(8, 4, 0);
+    case 16: return FC_R(16, 5, 0);
+    case 32: return FC_R(32, 6, 0);
+    case 64: return FC_R(64, 7, 0);
     default: break;
     }
-    if (tab.W < 32) return launch_reduce_w<Tab, 0, 5>(tab, G, u, resid, out, partials, s);
-    if (tab.W < 128) return launch_reduce_w<Tab, 0, 7>(tab, G, u, resid, out, partials, s);
-    return launch_reduce_w<Tab, 0, 12>(tab, G, u, resid, out, partials, s);
+    if (tab.W < 32) return FC_R(0, 5, 0);
+    if (tab.W < 128) return FC_R(0, 7, 0);
+    return FC_R(0, 12, 0);
+#undef FC_R
 }
 
 template cudaError_t launch_reduce<TableS>(const TableS &, const UnitGeom &,
                                            float, const float *, float *,
-                                           float *, cudaStream_t, int);
+                                           float *, cudaStream_t, int, int64_t,
+                                           int64_t);
 template cudaError_t launch_reduce<TableL>(const TableL &, const UnitGeom &,
                                            float, const float *, float *,
-                                           float *, cudaStream_t, int);
+                                           float *, cudaStream_t, int, int64_t,
+                                           int64_t);
 
 }  // namespace fc

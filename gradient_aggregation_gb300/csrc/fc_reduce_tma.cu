@@ -152,7 +152,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
                  float *partials, unsigned *err, const int64_t drop_tile,
-                 const uint64_t limit_ns)
+                 const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
@@ -163,8 +163,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const size_t gbytes = (size_t)W * ROW * 2;
     const size_t sbytes = gbytes + (size_t)TT * 4 + (MIS ? kMaxPieces * sizeof(int4) : 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t N = G.N;
-    const int64_t ntiles = (N + TT - 1) / TT;
+    // tiles of TT fused elements from f_begin (a multiple of 256) to f_end
+    const int64_t ntiles = (f_end - f_begin + TT - 1) / TT;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -190,8 +190,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 break;
             }
             if (t == drop_tile) continue;
-            const int64_t f0 = t * TT;
-            const int64_t f1 = f0 + TT < N ? f0 + TT : N;
+            const int64_t f0 = f_begin + t * TT;
+            const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
             const uint32_t full = smem_u32(&bars[s]);
             unsigned char *st = stages + (size_t)s * sbytes;
             const uint32_t rbytes = resid ? (uint32_t)((f1 - f0) * 4) : 0u;
@@ -276,8 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) atomicOr(err, 4u);
             return;
         }
-        const int64_t f0 = t * TT;
-        const int64_t f1 = f0 + TT < N ? f0 + TT : N;
+        const int64_t f0 = f_begin + t * TT;
+        const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
         const unsigned char *st = stages + (size_t)s * sbytes;
         for (int64_t lo = f0 + (int64_t)warp * FC_UNIT; lo < f1;
              lo += (int64_t)kConsumerWarps * FC_UNIT) {
@@ -396,7 +396,7 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
 template <class Tab, int WT, int MAXH, bool MIS>
 static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                                 const float *resid, float *out, float *partials,
-                                unsigned *err, cudaStream_t s)
+                                unsigned *err, cudaStream_t s, int64_t fb, int64_t fe)
 {
     int TT, S;
     size_t smem;
@@ -416,23 +416,23 @@ static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
             attr_set[dev] = true;
         }
     }
-    const int64_t tiles = (G.N + TT - 1) / TT;
+    const int64_t tiles = (fe - fb + TT - 1) / TT;
     const int grid = grid_for((const void *)kern, kThreads, smem, tiles);
     const int64_t drop = g_drop_tile.exchange(-1);
     const uint64_t limit = drop >= 0 ? g_drop_limit_ns.load() : kWaitLimitNs;
     return launch_after_prior(kern, (unsigned)grid, kThreads, smem, s, tab, G, TT, S, u,
-                              resid, out, partials, err, drop, limit);
+                              resid, out, partials, err, drop, limit, fb, fe);
 }
 
 template <class Tab, bool MIS>
 static cudaError_t launch_tma_layout(const Tab &tab, const UnitGeom &G, float u,
                                      const float *resid, float *out, float *partials,
-                                     unsigned *err, cudaStream_t s)
+                                     unsigned *err, cudaStream_t s, int64_t fb, int64_t fe)
 {
     switch (tab.W) {
-    case 4: return launch_tma_w<Tab, 4, 3, MIS>(tab, G, u, resid, out, partials, err, s);
-    case 8: return launch_tma_w<Tab, 8, 4, MIS>(tab, G, u, resid, out, partials, err, s);
-    case 16: return launch_tma_w<Tab, 16, 5, MIS>(tab, G, u, resid, out, partials, err, s);
+    case 4: return launch_tma_w<Tab, 4, 3, MIS>(tab, G, u, resid, out, partials, err, s, fb, fe);
+    case 8: return launch_tma_w<Tab, 8, 4, MIS>(tab, G, u, resid, out, partials, err, s, fb, fe);
+    case 16: return launch_tma_w<Tab, 16, 5, MIS>(tab, G, u, resid, out, partials, err, s, fb, fe);
     default: break;
     }
     return cudaErrorNotSupported;
@@ -441,12 +441,16 @@ static cudaError_t launch_tma_layout(const Tab &tab, const UnitGeom &G, float u,
 template <class Tab>
 cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
                               const float *resid, float *out, float *partials,
-                              unsigned *err, cudaStream_t s, int layout)
+                              unsigned *err, cudaStream_t s, int layout, int64_t fb,
+                              int64_t fe)
 {
+    if (fe < 0) fe = G.N;
+    if (fb >= fe) return cudaSuccess;
+    if (fb % FC_UNIT != 0) return cudaErrorInvalidValue;
     if (layout == 1)
-        return launch_tma_layout<Tab, false>(tab, G, u, resid, out, partials, err, s);
+        return launch_tma_layout<Tab, false>(tab, G, u, resid, out, partials, err, s, fb, fe);
     if (layout == 2)
-        return launch_tma_layout<Tab, true>(tab, G, u, resid, out, partials, err, s);
+        return launch_tma_layout<Tab, true>(tab, G, u, resid, out, partials, err, s, fb, fe);
     return cudaErrorNotSupported;
 }
 
@@ -467,9 +471,11 @@ template int tma_layout<TableS>(const TableS &, const UnitGeom &, const float *)
 template int tma_layout<TableL>(const TableL &, const UnitGeom &, const float *);
 template cudaError_t launch_reduce_tma<TableS>(const TableS &, const UnitGeom &, float,
                                                const float *, float *, float *,
-                                               unsigned *, cudaStream_t, int);
+                                               unsigned *, cudaStream_t, int, int64_t,
+                                               int64_t);
 template cudaError_t launch_reduce_tma<TableL>(const TableL &, const UnitGeom &, float,
                                                const float *, float *, float *,
-                                               unsigned *, cudaStream_t, int);
+                                               unsigned *, cudaStream_t, int, int64_t,
+                                               int64_t);
 
 }  // namespace fc

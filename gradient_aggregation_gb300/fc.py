@@ -48,6 +48,9 @@ _SIGS = {
     "fc_step_reduce_ordered": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _I32,
                                               _P, _SZ, _P]),
     "fc_step_reduce_kernel": (_I32, [_P, _I32, _I32, _P, _I64, _I32]),
+    "fc_step_reduce_span": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _I64, _I64,
+                                           _P, _SZ, _P]),
+    "fc_unit_start": (_I64, [_I64, _I64, _I64]),
     "fc_chunk_norms": (ctypes.c_int, [_P, _I64, _I64, _P, _P]),
     "fc_chunk_select": (ctypes.c_int, [_P, _I64, _I64, _P, _I64, _I64, _P, _P, _P, _P, _F32,
                                        _P, _P]),
@@ -261,6 +264,42 @@ def fc_step_reduce_ordered(grads, loss_scale: float, chunk: int,
                                         _p(workspace), workspace.numel(), _s(stream)))
 
 
+def fc_step_reduce_span(grads, loss_scale: float, chunk: int,
+                        residual: Optional[torch.Tensor], a: torch.Tensor, f_begin: int,
+                        f_end: int, workspace: torch.Tensor, stream=None) -> None:
+    t = _table(grads)
+    _check(lib().fc_step_reduce_span(t.ptrs, t.W, t.L, t.sizes_c, float(loss_scale),
+                                     int(chunk), _p(residual), _p(a), int(f_begin), int(f_end),
+                                     _p(workspace), workspace.numel(), _s(stream)))
+
+
+def fc_unit_start(N: int, chunk: int, f: int) -> int:
+    return int(lib().fc_unit_start(int(N), int(chunk), int(f)))
+
+
+def layer_group_spans(sizes: Sequence[int], chunk: int,
+                      groups: Sequence[Tuple[int, int]]) -> List[Tuple[int, int]]:
+    """Spans for fc_step_reduce_span, one per layer group [first, end) in
+    the order the groups' gradients become ready.  The groups must tile the
+    layers and arrive last layer first or first layer first."""
+    off, N = fc_layout(sizes)
+    off = off + [N]
+    rng = [(off[a], off[b]) for a, b in groups]
+    if not rng:
+        raise ValueError("no layer groups")
+    if sorted(rng) != sorted(set(rng)) or any(a > b for a, b in rng):
+        raise ValueError("layer groups must be disjoint ranges")
+    srt = sorted(rng)
+    if srt[0][0] != 0 or srt[-1][1] != N or any(srt[i][1] != srt[i + 1][0]
+                                                  for i in range(len(srt) - 1)):
+        raise ValueError("layer groups must cover every layer once")
+    if rng == srt:                       # first layer first
+        return [(fc_unit_start(N, chunk, a), fc_unit_start(N, chunk, b)) for a, b in rng]
+    if rng == srt[::-1]:                 # last layer first (backprop order)
+        return list(rng)
+    raise ValueError("layer groups must arrive in layer order or in reverse layer order")
+
+
 def fc_step_reduce_kernel(grads, chunk: int, order: int = FC_ORDER_TREE) -> int:
     """FC_REDUCE_* of the phase-1 kernel the library picks for this layout
     (host only; `grads` is [worker][layer] tensors or a PtrTable, which
@@ -386,6 +425,26 @@ class Engine:
                                      self.weights_fp16, self.mask, self.packed,
                                      self.workspace, self.packed_fp16, self.send_scale,
                                      stream)
+
+    def step_layer_groups(self, grads, groups: Sequence[Tuple[int, int]],
+                          ready: Optional[Sequence[torch.cuda.Event]] = None,
+                          stream=None) -> None:
+        """One step with phase 1 streamed per layer group: `groups` lists
+        layer ranges [first, end) in the order their gradients become ready
+        (backprop: last layer first); before reducing group i the stream
+        waits for ready[i], if given.  Results are the bits of step()."""
+        spans = layer_group_spans(self.sizes, self.chunk, groups)
+        s = stream if stream is not None else torch.cuda.current_stream()
+        for i, (fb, fe) in enumerate(spans):
+            if ready is not None:
+                s.wait_event(ready[i])
+            fc_step_reduce_span(grads, self.loss_scale, self.chunk, self.residual, self.a,
+                                fb, fe, self.workspace, s)
+        fc_step_select(self.N, self.chunk, self.k, self.norms, self.idx, self.mask,
+                       self.threshold, self.workspace, s)
+        fc_step_update(self.a, self.N, self.chunk, self.lr, self.momentum, self.residual,
+                       self.velocity, self.weights, self.weights_fp16, self.mask, self.packed,
+                       self.workspace, self.packed_fp16, self.send_scale, s)
 
     def state_dict(self) -> dict:
         return {"residual": self.residual.clone(), "velocity": self.velocity.clone(),

@@ -251,6 +251,38 @@ FC_API fc_status fc_step_reduce_ordered(const void *const *grads, int32_t W,
                                         int32_t order, void *workspace,
                                         size_t workspace_bytes, void *stream);
 
+/* Phase 1 on a span of the fused vector, so that the reduction of early
+ * layer groups overlaps the arrival of later ones (GradientFlow abstract:
+ * computation/communication overlap; backprop hands the layers over last
+ * layer first).  Reduces exactly the 256-element units (unit = up to 256
+ * elements of one chunk, the j-th starting at chunk start + 256 j) whose
+ * first element lies in [f_begin, f_end): `a` for every element of those
+ * units and their sums of squares in the workspace, as fc_step_reduce
+ * does.  Calls whose spans partition [0, N) leave `a` and the workspace
+ * exactly as one fc_step_reduce call does (same bits, any call order);
+ * fc_step_select and fc_step_update then finish the step.
+ *  A unit that starts in the span may end up to 255 elements after f_end
+ *  (never past its chunk), so every layer overlapping
+ *  [f_begin, fc_unit_start of the span's last unit + 256) must hold its
+ *  gradients when the call runs on the stream.  For layer groups arriving
+ *  last layer first, [group start, group end) is such a span; for groups
+ *  arriving first layer first, [fc_unit_start(group start),
+ *  fc_unit_start(group end)) is.
+ *  Tree order only.  0 <= f_begin <= f_end <= N, else FC_ERR_INVALID_ARG;
+ *  an empty span launches nothing.  Other arguments as fc_step_reduce. */
+FC_API fc_status fc_step_reduce_span(const void *const *grads, int32_t W,
+                                     int32_t L, const int64_t *sizes,
+                                     float loss_scale, int64_t chunk,
+                                     const float *residual, float *a,
+                                     int64_t f_begin, int64_t f_end,
+                                     void *workspace, size_t workspace_bytes,
+                                     void *stream);
+
+/* First element of the unit (see fc_step_reduce_span) that holds fused
+ * element f: chunk start + 256 * floor(offset in chunk / 256), for
+ * 0 <= f < N; N for f == N; -1 for any other argument. */
+FC_API int64_t fc_unit_start(int64_t N, int64_t chunk, int64_t f);
+
 /* Which phase-1 kernel fc_step_reduce_ordered (and so fc_step) launches for
  * this layout of gradients (arguments as there; chunk > 0, order an
  * FC_ORDER_* value).  Host only: the pointers are compared, never read, and

@@ -169,3 +169,68 @@ def test_reduce_kernel_choice_from_layout(fc_lib):
         k(separate(8, even), 0)
     with pytest.raises(fc.FcError):
         k(separate(8, even, lambda w, l: 1), 256)                          # odd address
+
+
+def _unit_starts(N, chunk):
+    """Unit starts by their definition: each chunk cut into 256-element units."""
+    starts = []
+    for c0 in range(0, N, chunk):
+        starts.extend(range(c0, min(c0 + chunk, N), 256))
+    return starts
+
+
+def test_unit_start_matches_the_unit_definition(fc_lib):
+    from gradient_aggregation_gb300 import fc
+    for N, chunk in [(1, 1), (1000, 64), (5000, 300), (70000, 32768), (4096, 4096), (9999, 256)]:
+        starts = _unit_starts(N, chunk)
+        for f in range(0, N, max(1, N // 997)):
+            assert fc.fc_unit_start(N, chunk, f) == max(x for x in starts if x <= f)
+        assert fc.fc_unit_start(N, chunk, N) == N
+    assert fc.fc_unit_start(10, 4, 11) == -1
+    assert fc.fc_unit_start(10, 0, 1) == -1
+    assert fc.fc_unit_start(10, 4, -1) == -1
+
+
+def test_layer_group_spans_own_every_unit_once_when_ready(fc_lib):
+    """The spans of a layer grouping give every unit to exactly one call, and
+    only once every layer the unit touches has arrived."""
+    from gradient_aggregation_gb300 import fc
+    sizes = [1001, 64, 3333, 2, 700, 5000]
+    off, N = fc.fc_layout(sizes)
+    off = off + [N]
+    groupings = [[(4, 6), (2, 4), (0, 2)], [(0, 1), (1, 5), (5, 6)], [(0, 6)],
+                 [(5, 6), (4, 5), (3, 4), (2, 3), (1, 2), (0, 1)],
+                 [(0, 1), (1, 2), (2, 3), (3, 4), (4, 5), (5, 6)]]
+    for chunk in (256, 300, 1024, 20000):
+        starts = _unit_starts(N, chunk)
+        for groups in groupings:
+            spans = fc.layer_group_spans(sizes, chunk, groups)
+            owned = [[x for x in starts if a <= x < b] for a, b in spans]
+            assert sorted(sum(owned, [])) == starts
+            ready = []
+            for (ga, gb), own in zip(groups, owned):
+                ready.append((off[ga], off[gb]))
+                for x in own:
+                    last = min(x + 256, (x // chunk + 1) * chunk, N) - 1
+                    for f in (x, last):
+                        assert any(a <= f < b for a, b in ready), (chunk, groups, x)
+    with pytest.raises(ValueError):
+        fc.layer_group_spans(sizes, 256, [(0, 3), (2, 6)])            # overlap
+    with pytest.raises(ValueError):
+        fc.layer_group_spans(sizes, 256, [(0, 3)])                    # missing layers
+    with pytest.raises(ValueError):
+        fc.layer_group_spans(sizes, 256, [(2, 4), (0, 2), (4, 6)])    # neither order
+
+
+def test_span_arguments_are_checked_before_device_work(fc_lib):
+    from gradient_aggregation_gb300 import fc
+    P = ctypes.c_void_p
+    fake = 0x10000
+    arr = (ctypes.c_void_p * 4)(*([fake] * 4))
+    g = ctypes.cast(arr, P)
+    sizes = (ctypes.c_int64 * 2)(8, 8)
+    sp = lambda b, e: int(fc_lib.fc_step_reduce_span(g, 2, 2, ctypes.cast(sizes, P), 1.0, 4, None,
+                                                     fake, b, e, fake, 10 ** 6, None))
+    assert sp(-1, 4) == fc.FC_ERR_INVALID_ARG
+    assert sp(5, 4) == fc.FC_ERR_INVALID_ARG
+    assert sp(0, 17) == fc.FC_ERR_INVALID_ARG and b"span" in fc_lib.fc_last_error()

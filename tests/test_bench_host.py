@@ -77,3 +77,17 @@ def test_phase1_kernel_choice_and_profile_parsing():
     assert bench.traffic_from_profile("not-the-current-source", wl) is None
     t = bench.traffic_from_profile(bench.kernel_source_hash(), wl)
     assert t is None or 2.0e9 < t < 3.0e9
+
+
+def test_layer_groups_reverse_tile_the_layers_last_first(fc_lib):
+    from gradient_aggregation_gb300 import fc, workload
+    for name in ("tiny", "nin", "googlenet", "alexnet", "stress"):
+        wl = workload.get(name)
+        g = bench.layer_groups_reverse(wl.sizes, 4)
+        assert g[0][1] == wl.L and g[-1][0] == 0
+        assert all(a < b for a, b in g) and all(g[i][0] == g[i + 1][1] for i in range(len(g) - 1))
+        assert 1 <= len(g) <= 4
+        assert fc.layer_group_spans(wl.sizes, wl.chunk, g) == [
+            (sum(wl.sizes[:a]), sum(wl.sizes[:b])) for a, b in g]
+    # AlexNet: fc8+fc7, fc6, the convolutions (fc6 alone passes two marks)
+    assert bench.layer_groups_reverse(workload.get("alexnet").sizes, 4) == [(12, 16), (10, 12), (0, 10)]

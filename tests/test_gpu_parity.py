@@ -504,3 +504,81 @@ def test_bucketed_gradients_merge_into_one_segment():
         a, b = sep.snapshot(), buck.snapshot()
         _compare_paths(a, b)
         oracle_step(g_np, st, wl, b)
+
+
+def _engine(wl):
+    w0 = torch.from_numpy(workload.initial_weights(wl)).cuda()
+    return fc.Engine(wl.sizes, wl.W, wl.chunk, wl.keep_percent, 100, wl.loss_scale, wl.lr,
+                     wl.momentum, w0, want_fp16=True, want_packed=True,
+                     want_packed_fp16=True, send_scale=wl.loss_scale)
+
+
+def _engine_bits(e):
+    return {k: getattr(e, k).cpu().numpy() for k in
+            ("residual", "velocity", "weights", "weights_fp16", "norms", "idx", "mask",
+             "packed", "packed_fp16", "threshold")}
+
+
+def _groupings(L, rng):
+    cuts = sorted(rng.choice(np.arange(1, L), size=min(2, L - 1), replace=False)) if L > 1 else []
+    b = [0] + [int(c) for c in cuts] + [L]
+    three = [(b[i], b[i + 1]) for i in range(len(b) - 1)]
+    per_layer = [(l, l + 1) for l in range(L)]
+    return [three[::-1], three, per_layer[::-1], [(0, L)]]
+
+
+SPAN_CASES = {
+    "googlenet": None, "nin": None, "tiny": None,
+    "aligned16": dict(W=16, sizes=[12288, 808, 8, 60000, 8000], chunk=1024, keep_percent=20),
+    "register5": dict(W=5, sizes=[1001, 64, 3333, 2, 700], chunk=300, keep_percent=30),
+}
+
+
+@pytest.mark.parametrize("name", list(SPAN_CASES))
+def test_layer_group_streaming_matches_fc_step(name):
+    """Phase 1 streamed per layer group (fc_step_reduce_span), in backprop
+    order and in layer order, gives the bits of fc_step."""
+    kw = SPAN_CASES[name]
+    wl = workload.get(name) if kw is None else workload.custom(config_id=170, steps=2, **kw)
+    rng = np.random.default_rng(11)
+    groupings = _groupings(wl.L, rng)
+    ref = _engine(wl)
+    runs = [_engine(wl) for _ in groupings]
+    for s in range(2):
+        g_dev = dev_grads(workload.all_grads(wl, s))
+        ref.step(g_dev)
+        for eng, groups in zip(runs, groupings):
+            eng.step_layer_groups(g_dev, groups)
+        want = _engine_bits(ref)
+        for eng, groups in zip(runs, groupings):
+            got = _engine_bits(eng)
+            for k in want:
+                assert bits_equal(got[k], want[k]), (name, groups, k)
+
+
+def test_layer_group_streaming_waits_for_each_group():
+    """Gradients copied in group by group (last layer first) on another
+    stream, each span waiting only for its own group's event."""
+    wl = workload.get("googlenet")
+    groups = [(40, 57), (20, 40), (0, 20)]
+    ref, eng = _engine(wl), _engine(wl)
+    src = dev_grads(workload.all_grads(wl, 0))
+    dst = [[torch.full_like(t, float("nan")) for t in row] for row in src]
+    ref.step(src)
+    copy, comp = torch.cuda.Stream(), torch.cuda.Stream()
+    copy.wait_stream(torch.cuda.current_stream())
+    comp.wait_stream(torch.cuda.current_stream())
+    ready = []
+    with torch.cuda.stream(copy):
+        for a, b in groups:
+            for w in range(wl.W):
+                for l in range(a, b):
+                    dst[w][l].copy_(src[w][l], non_blocking=True)
+            ev = torch.cuda.Event()
+            ev.record(copy)
+            ready.append(ev)
+    eng.step_layer_groups(dst, groups, ready=ready, stream=comp)
+    torch.cuda.synchronize()
+    want, got = _engine_bits(ref), _engine_bits(eng)
+    for k in want:
+        assert bits_equal(got[k], want[k]), k
