@@ -256,6 +256,24 @@ def layer_groups_reverse(sizes, n_groups):
     return groups
 
 
+def group_major_layout(sizes, W, groups):
+    """Buffer layout [group][worker][group's elements], groups in arrival
+    order: the [begin, end) of each group in the buffer, and the position of
+    every (worker, layer) tensor."""
+    off = [0]
+    for n in sizes:
+        off.append(off[-1] + n)
+    span, pos, acc = [], [[0] * len(sizes) for _ in range(W)], 0
+    for a, b in groups:
+        glen = off[b] - off[a]
+        span.append((acc, acc + W * glen))
+        for w in range(W):
+            for l in range(a, b):
+                pos[w][l] = acc + w * glen + off[l] - off[a]
+        acc += W * glen
+    return span, pos
+
+
 def traffic_from_profile(src_hash, wl):
     """DRAM bytes per launch of the reduction kernel from the committed ncu
     summary, if it was taken on the current kernel source."""
@@ -435,29 +453,40 @@ def run_gpu(args, wl, rank, world, local):
         bounds = [len(hv) * i // 4 for i in range(5)]
         parts = [(host[bounds[i]:bounds[i + 1]], stage[bounds[i]:bounds[i + 1]])
                  for i in range(4)]
-        # (d): backprop order, last layer first: each layer group's rows are
-        # copied in on their own stream, and phase 1 reduces the group's span
-        # as soon as its copy has landed (fc_step_reduce_span)
+        # (d): backprop order, last layer first.  The buffers are laid out
+        # group-major ([group][worker][group's elements]) so that each layer
+        # group arrives with one copy on its own stream, and phase 1 reduces
+        # the group's span as soon as its copy has landed (fc_step_reduce_span)
         groups = layer_groups_reverse(wl.sizes, 4)
         group_stream = torch.cuda.Stream(device=dev)
-        off_l, _ = fc.fc_layout(wl.sizes)
-        off_l = off_l + [N]
-        group_parts = [[(host[w * N + off_l[a]: w * N + off_l[b]],
-                         stage[w * N + off_l[a]: w * N + off_l[b]]) for w in range(W)]
-                       for a, b in groups]
+        gspan, gpos = group_major_layout(wl.sizes, W, groups)
+        group_parts = [(host[a:b], stage[a:b]) for a, b in gspan]
+
+        def group_views(buf):
+            return [[buf[gpos[w][l]: gpos[w][l] + wl.sizes[l]] for l in range(wl.L)]
+                    for w in range(W)]
+
+        def fill_group_major():
+            for w in range(W):
+                for l in range(wl.L):
+                    hv[gpos[w][l]: gpos[w][l] + wl.sizes[l]] = grads_np[w][l]
+
         variants = {}
-        for name, table, copy_in in (("copy_engine", fc.PtrTable(views(stage)), 1),
-                                     ("copy_engine_x4", fc.PtrTable(views(stage)), 4),
-                                     ("layer_groups", fc.PtrTable(views(stage)), 2),
-                                     ("zero_copy", fc.PtrTable(views(host)), 0)):
+        for name, copy_in in (("copy_engine", 1), ("copy_engine_x4", 4), ("zero_copy", 0),
+                              ("layer_groups", 2)):
+            if copy_in == 2:
+                fill_group_major()
+                table = fc.PtrTable(group_views(stage))
+            else:
+                table = fc.PtrTable(views(host if copy_in == 0 else stage))
+
             def one_step():
                 if copy_in == 2:
                     group_stream.wait_stream(s)     # the previous step is done with `stage`
                     ready = []
                     with torch.cuda.stream(group_stream):
-                        for part in group_parts:
-                            for hpart, dpart in part:
-                                dpart.copy_(hpart, non_blocking=True)
+                        for hpart, dpart in group_parts:
+                            dpart.copy_(hpart, non_blocking=True)
                             ev = torch.cuda.Event()
                             ev.record(group_stream)
                             ready.append(ev)
@@ -506,10 +535,10 @@ def run_gpu(args, wl, rank, world, local):
                                        "gradients, then fc_step",
                         "copy_engine_x4": "the pinned-host -> device copy of all workers' "
                                           "gradients split over four streams, then fc_step",
-                        "layer_groups": "layer groups copied in last layer first on a copy "
-                                        "stream, phase 1 reducing each group's span as soon "
-                                        "as its copy lands (fc_step_reduce_span), then "
-                                        "select + update",
+                        "layer_groups": "layer groups copied in last layer first, one copy "
+                                        "per group on a copy stream, phase 1 reducing each "
+                                        "group's span as soon as its copy lands "
+                                        "(fc_step_reduce_span), then select + update",
                         "zero_copy": "fc_step reading the pinned host gradients in place "
                                      "over the CPU-GPU link"}[best]
                        + "; kept indices + threshold copied back and read on the host",

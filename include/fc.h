@@ -295,7 +295,9 @@ FC_API int64_t fc_unit_start(int64_t N, int64_t chunk, int64_t f);
  *                            for every worker (4, 8 or 16 workers);
  *  FC_REDUCE_STAGED_SHIFTED  the same for layers at any offset whose address
  *                            modulo 16 bytes, at a given fused index, is the
- *                            same for every worker. */
+ *                            same for every worker; also taken by aligned
+ *                            layouts of at least 8192 tiles of 2048
+ *                            elements, where it measured faster. */
 #define FC_REDUCE_REGISTER 0
 #define FC_REDUCE_STAGED 1
 #define FC_REDUCE_STAGED_SHIFTED 2

@@ -147,6 +147,9 @@ def test_reduce_kernel_choice_from_layout(fc_lib):
     even, odd = [4096, 800, 8], [1001, 64, 3333, 2]       # N = 4904, 4400
     k = fc.fc_step_reduce_kernel
     assert k(separate(16, even), 256) == fc.FC_REDUCE_STAGED
+    # aligned but long (at least 8192 tiles of 2048): the shifted variant
+    assert k(separate(16, [8192 * 2048]), 256) == fc.FC_REDUCE_STAGED_SHIFTED
+    assert k(separate(16, [8191 * 2048]), 256) == fc.FC_REDUCE_STAGED
     assert k(separate(8, odd), 512) == fc.FC_REDUCE_STAGED_SHIFTED
     assert k(separate(4, odd), 256) == fc.FC_REDUCE_STAGED_SHIFTED
     # a bucket per worker is one aligned segment, whatever the layer sizes

@@ -68,7 +68,9 @@ def test_reference_arm_line_and_other_ranks():
 
 def test_phase1_kernel_choice_and_profile_parsing():
     from gradient_aggregation_gb300 import workload
-    assert bench.phase1_kernel(workload.get("alexnet")) == "k_reduce_tma"
+    # aligned, and long enough that the shifted variant is the faster one
+    assert bench.phase1_kernel(workload.get("alexnet")) == "k_reduce_tma, shifted layout"
+    assert bench.phase1_kernel(workload.get("tiny")) == "k_reduce_tma"
     assert bench.phase1_kernel(workload.get("stress")) == "k_reduce"      # 64 workers
     # layers at odd offsets, one address shift per layer for all workers
     assert bench.phase1_kernel(workload.get("googlenet")) == "k_reduce_tma, shifted layout"
@@ -91,3 +93,19 @@ def test_layer_groups_reverse_tile_the_layers_last_first(fc_lib):
             (sum(wl.sizes[:a]), sum(wl.sizes[:b])) for a, b in g]
     # AlexNet: fc8+fc7, fc6, the convolutions (fc6 alone passes two marks)
     assert bench.layer_groups_reverse(workload.get("alexnet").sizes, 4) == [(12, 16), (10, 12), (0, 10)]
+
+
+def test_group_major_layout_places_each_group_in_one_block():
+    sizes, W = [5, 3, 7, 2], 3
+    groups = [(2, 4), (0, 2)]
+    span, pos = bench.group_major_layout(sizes, W, groups)
+    assert span == [(0, 27), (27, 51)]
+    buf = [None] * 51
+    for w in range(W):
+        for l, n in enumerate(sizes):
+            for j in range(n):
+                assert buf[pos[w][l] + j] is None
+                buf[pos[w][l] + j] = (w, l, j)
+    assert None not in buf
+    for (a, b), (lo, hi) in zip(groups, span):      # a group's block holds its layers only
+        assert {buf[i][1] for i in range(lo, hi)} == set(range(a, b))

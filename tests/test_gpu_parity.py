@@ -58,7 +58,7 @@ def _run_workload(wl, steps=None, both_paths=True, expect_kernel=None, to_dev=de
 
 
 WORKLOAD_KERNEL = {"tiny": fc.FC_REDUCE_STAGED, "nin": fc.FC_REDUCE_STAGED_SHIFTED,
-                   "googlenet": fc.FC_REDUCE_STAGED_SHIFTED, "alexnet": fc.FC_REDUCE_STAGED,
+                   "googlenet": fc.FC_REDUCE_STAGED_SHIFTED, "alexnet": fc.FC_REDUCE_STAGED_SHIFTED,
                    "stress": fc.FC_REDUCE_REGISTER}
 
 
