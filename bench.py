@@ -476,9 +476,9 @@ def run_gpu(args, wl, rank, world, local):
                               ("layer_groups", 2)):
             if copy_in == 2:
                 fill_group_major()
-                table = fc.PtrTable(group_views(stage))
+                e_table = fc.PtrTable(group_views(stage))
             else:
-                table = fc.PtrTable(views(host if copy_in == 0 else stage))
+                e_table = fc.PtrTable(views(host if copy_in == 0 else stage))
 
             def one_step():
                 if copy_in == 2:
@@ -490,7 +490,7 @@ def run_gpu(args, wl, rank, world, local):
                             ev = torch.cuda.Event()
                             ev.record(group_stream)
                             ready.append(ev)
-                    eng.step_layer_groups(table, groups, ready=ready, stream=s)
+                    eng.step_layer_groups(e_table, groups, ready=ready, stream=s)
                     with torch.cuda.stream(s):
                         res_idx.copy_(eng.idx, non_blocking=True)
                         res_thr.copy_(eng.threshold, non_blocking=True)
@@ -506,7 +506,7 @@ def run_gpu(args, wl, rank, world, local):
                             dpart.copy_(hpart, non_blocking=True)
                     for cs in copy_streams:
                         s.wait_stream(cs)
-                eng.step(table, s)
+                eng.step(e_table, s)
                 with torch.cuda.stream(s):
                     res_idx.copy_(eng.idx, non_blocking=True)
                     res_thr.copy_(eng.threshold, non_blocking=True)
