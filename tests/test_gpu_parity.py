@@ -582,3 +582,34 @@ def test_layer_group_streaming_waits_for_each_group():
     want, got = _engine_bits(ref), _engine_bits(eng)
     for k in want:
         assert bits_equal(got[k], want[k]), k
+
+
+def _counter_words(ws, N, chunk):
+    """The first four 32-bit words of the pipeline workspace's counter block
+    (after the fp32 unit sums, at a 256-byte boundary)."""
+    C = -(-N // chunk)
+    U = -(-chunk // 256)
+    units = (C - 1) * U + -(-(N - (C - 1) * chunk) // 256)
+    off = -(-units * 4 // 256) * 256
+    return ws[off: off + 16].cpu().numpy().view(np.uint32)
+
+
+@pytest.mark.parametrize("name", ["googlenet", "tiny", "aligned16"])
+def test_pipeline_leaves_its_counters_at_zero(name):
+    """The workspace's counter block (the selection's count of finished
+    blocks, the staged reduction's error word) is zero again after whole
+    steps and after steps streamed per layer group: a workspace zeroed once
+    serves every later step."""
+    kw = SPAN_CASES.get(name)
+    wl = workload.get(name) if kw is None else workload.custom(config_id=171, steps=1, **kw)
+    g = dev_grads(workload.all_grads(wl, 0))
+    assert fc.fc_step_reduce_kernel(g, wl.chunk) != fc.FC_REDUCE_REGISTER
+    eng = _engine(wl)
+    for _ in range(3):
+        eng.step(g)
+    torch.cuda.synchronize()
+    assert not _counter_words(eng.workspace, eng.N, eng.chunk).any()
+    groups = [(wl.L // 2, wl.L), (0, wl.L // 2)] if wl.L > 1 else [(0, 1)]
+    eng.step_layer_groups(g, groups)
+    torch.cuda.synchronize()
+    assert not _counter_words(eng.workspace, eng.N, eng.chunk).any()
