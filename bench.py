@@ -527,8 +527,23 @@ def run_gpu(args, wl, rank, world, local):
             et = max_t(e0.elapsed_time(e1) / 1e3)
             variants[name] = {"value": round(replica_value(world, step_bytes, E, et), 3),
                               "ms_per_step": round(et * 1e3 / E, 4), "steps": E}
+        # the link itself: the same bytes copied host -> device, nothing else
+        with torch.cuda.stream(s):
+            stage.copy_(host, non_blocking=True)
+        torch.cuda.synchronize()
+        l0, l1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        l0.record(s)
+        with torch.cuda.stream(s):
+            for _ in range(3):
+                stage.copy_(host, non_blocking=True)
+        l1.record(s)
+        torch.cuda.synchronize()
+        link_gbs = W * N * 2 * 3 / (l0.elapsed_time(l1) / 1e3) / 1e9
         best = max(variants, key=lambda k: variants[k]["value"])
         e2e = {"value": variants[best]["value"], "unit": UNIT,
+               "link": {"h2d_copy_gbs": round(link_gbs, 1),
+                        "frac": round(variants[best]["value"] / link_gbs, 4),
+                        "note": "pinned host -> device copy of the step's gradients alone"},
                "h2d_bytes_per_step": W * N * 2, "d2h_bytes_per_step": 4 * eng.k + 4,
                "steps": variants[best]["steps"], "ms_per_step": variants[best]["ms_per_step"],
                "path": {"copy_engine": "one pinned-host -> device copy of all workers' "

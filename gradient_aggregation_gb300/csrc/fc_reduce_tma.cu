@@ -26,7 +26,10 @@
 //    and records the pieces in a small table in the stage.  A consumer reads
 //    its 8 elements with two 16-byte shared-memory loads and a funnel shift;
 //    only groups not fully inside one copied piece (at layer boundaries)
-//    read their elements from global memory.
+//    read their elements from global memory.  Aligned layouts long enough
+//    (FC_TMA_SHIFTED_MIN_TILES) also take this variant, with every shift 0:
+//    it measured faster on long runs.  Aligned mid-size runs go to the
+//    register kernel instead (see tma_layout).
 //
 // Every wait on an mbarrier gives up after a time limit (read from the
 // global timer); the kernel then records the failure in `err` and returns,
@@ -116,9 +119,14 @@ constexpr uint64_t kWaitLimitNs = 2000000000ull;  // 2 s: far beyond any tile
 // from global memory by the consumers).
 constexpr int kSlack = 64;
 
-// Aligned layouts of at least this many tiles take the shifted variant.
+// Aligned layouts of at least FC_TMA_SHIFTED_MIN_TILES tiles take the
+// shifted variant; from FC_TMA_REGISTER_MIN_TILES up to that, the register
+// kernel; shorter ones the aligned variant.
 #ifndef FC_TMA_SHIFTED_MIN_TILES
 #define FC_TMA_SHIFTED_MIN_TILES 8192
+#endif
+#ifndef FC_TMA_REGISTER_MIN_TILES
+#define FC_TMA_REGISTER_MIN_TILES 1536
 #endif
 constexpr int kMaxPieces = 32;
 
@@ -396,12 +404,19 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
     tma_shape(tab.W, !aligned, TT, S, smem);
     if (S < 2) return 0;
     if (!aligned) return 2;
-    // The shifted variant also serves aligned layouts (every shift 0).  On
-    // long runs it measured faster (AlexNet-sized: 352 against 361 us), on
-    // short ones slower (7.6M elements: 34.5 against 30 us).
-    tma_shape(tab.W, true, TT, S, smem);
+    // Aligned layouts, by length (tiles of TT elements), as measured in
+    // isolation:
+    //  * long runs take the shifted variant (every shift 0): AlexNet-sized
+    //    352 against 361 us for the aligned variant;
+    //  * mid-size runs the register kernel streams faster than either
+    //    staged variant (7M elements x 16 workers: 43.5 against 48 us);
+    //  * short runs keep the aligned variant (2M x 16: 11 against 13 us).
     const int64_t tiles = (G.N + TT - 1) / TT;
-    return (S >= 2 && tiles >= FC_TMA_SHIFTED_MIN_TILES) ? 2 : 1;
+    if (tiles >= FC_TMA_SHIFTED_MIN_TILES) {
+        tma_shape(tab.W, true, TT, S, smem);
+        if (S >= 2) return 2;
+    }
+    return tiles >= FC_TMA_REGISTER_MIN_TILES ? 0 : 1;
 }
 
 template <class Tab, int WT, int MAXH, bool MIS>

@@ -292,12 +292,14 @@ FC_API int64_t fc_unit_start(int64_t N, int64_t chunk, int64_t f);
  *  FC_REDUCE_REGISTER        register streaming, one warp per 256-element unit;
  *  FC_REDUCE_STAGED          bulk copies staged in shared memory, every layer
  *                            at a multiple of 8 elements and 16-byte aligned
- *                            for every worker (4, 8 or 16 workers);
+ *                            for every worker (4, 8 or 16 workers), fewer
+ *                            than 1536 tiles of 2048 elements;
  *  FC_REDUCE_STAGED_SHIFTED  the same for layers at any offset whose address
  *                            modulo 16 bytes, at a given fused index, is the
  *                            same for every worker; also taken by aligned
- *                            layouts of at least 8192 tiles of 2048
- *                            elements, where it measured faster. */
+ *                            layouts of at least 8192 tiles.
+ * Aligned layouts from 1536 to 8191 tiles take FC_REDUCE_REGISTER: there it
+ * measured faster than either staged variant. */
 #define FC_REDUCE_REGISTER 0
 #define FC_REDUCE_STAGED 1
 #define FC_REDUCE_STAGED_SHIFTED 2

@@ -149,7 +149,13 @@ def test_reduce_kernel_choice_from_layout(fc_lib):
     assert k(separate(16, even), 256) == fc.FC_REDUCE_STAGED
     # aligned but long (at least 8192 tiles of 2048): the shifted variant
     assert k(separate(16, [8192 * 2048]), 256) == fc.FC_REDUCE_STAGED_SHIFTED
-    assert k(separate(16, [8191 * 2048]), 256) == fc.FC_REDUCE_STAGED
+    assert k(separate(16, [8191 * 2048]), 256) == fc.FC_REDUCE_REGISTER
+    # mid-size aligned runs stream faster in the register kernel
+    assert k(separate(16, [1536 * 2048]), 256) == fc.FC_REDUCE_REGISTER
+    assert k(separate(16, [1535 * 2048]), 256) == fc.FC_REDUCE_STAGED
+    assert k(separate(8, [1000, 3000 * 2048 - 1000]), 256) == fc.FC_REDUCE_REGISTER
+    # shifted layouts stay staged at any length
+    assert k(separate(16, [3001, 3000 * 2048 - 3001]), 256) == fc.FC_REDUCE_STAGED_SHIFTED
     assert k(separate(8, odd), 512) == fc.FC_REDUCE_STAGED_SHIFTED
     assert k(separate(4, odd), 256) == fc.FC_REDUCE_STAGED_SHIFTED
     # a bucket per worker is one aligned segment, whatever the layer sizes

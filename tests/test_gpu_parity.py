@@ -451,15 +451,19 @@ def test_select_with_only_the_fp16_send_buffer():
     assert bits_equal(p16.cpu().numpy().view(np.uint16), oracle.pack_fp16(packed_o, wl.loss_scale))
 
 
-def test_staged_reduction_reports_a_wait_that_runs_out():
+@pytest.mark.parametrize("sizes,kind", [
+    ([8192, 16384, 40960], fc.FC_REDUCE_STAGED),
+    ([8191, 16385, 40960], fc.FC_REDUCE_STAGED_SHIFTED)], ids=["aligned", "shifted"])
+def test_staged_reduction_reports_a_wait_that_runs_out(sizes, kind):
     """Failure path of the TMA-staged reduction, without any fault: the test
     hook makes the next launch issue no copies for tile 0, so the waits on it
     run out (20 ms limit).  The step reports it (NaN threshold, nothing kept,
     idx -1), the context stays usable, and the next steps match the oracle."""
-    wl = workload.custom(W=16, sizes=[8192, 16384, 40960], chunk=4096, keep_percent=25,
+    wl = workload.custom(W=16, sizes=sizes, chunk=4096, keep_percent=25,
                          config_id=220, steps=2)
     run = GpuRun(wl, "pipeline", inplace=True)
     g0 = dev_grads(workload.all_grads(wl, 0))
+    assert fc.fc_step_reduce_kernel(g0, wl.chunk) == kind
     fc.fc_test_stage_loss(0, 20_000_000)
     run.step(g0)
     snap = run.snapshot()
