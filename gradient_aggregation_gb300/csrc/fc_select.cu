@@ -177,16 +177,20 @@ __global__ void __launch_bounds__(SEL_THREADS)
             const float n = chunk_norm_from_units(G, partials, c, lane);
             if (lane == 0) norms[c] = n;
         }
-        __threadfence();  // publish this block's norms before counting it
+        // publish this block's norms before counting it: the writers fence,
+        // the barrier orders them before the count
+        if (lane == 0) __threadfence();
         __syncthreads();
         if (tid == 0) {
             const unsigned seen = atomicAdd(done, 1u);
             s_last = seen == gridDim.x - 1 ? 1u : 0u;
+            if (s_last) {
+                __threadfence();  // every block's norms, before this block reads them
+                *done = 0u;       // ready for the next call
+            }
         }
         __syncthreads();
         if (!s_last) return;
-        __threadfence();
-        if (tid == 0) *done = 0u;  // ready for the next call
         // A wait inside the staged reduction gave up (not expected to
         // happen): report it as a NaN threshold with nothing kept.
         if (err && __ldcg(err) != 0u) {
