@@ -424,6 +424,35 @@ def run_gpu(args, wl, rank, world, local):
     # followed by fc_step, (b) fc_step reading the pinned host buffer in
     # place over the CPU-GPU link, so the reduction consumes the gradients
     # as they arrive (the transfer and the reduction overlap).
+    # the same step captured once in a CUDA graph and replayed: no host work
+    # per step (the library's calls are capture-safe)
+    graph = None
+    try:
+        gs = torch.cuda.Stream(device=dev)
+        gs.wait_stream(s)
+        cg = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(cg, stream=gs):
+            eng.step(table)
+        with torch.cuda.stream(gs):
+            for _ in range(max(3, warmup)):
+                cg.replay()
+            KG = min(K, 1000)
+            g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            barrier()
+            g0.record(gs)
+            for _ in range(KG):
+                cg.replay()
+            g1.record(gs)
+        torch.cuda.synchronize()
+        gt = max_t(g0.elapsed_time(g1) / 1e3)
+        graph = {"value": round(replica_value(world, W * N * 2, KG, gt), 3), "unit": UNIT,
+                 "ms_per_step": round(gt * 1e3 / KG, 5), "steps": KG,
+                 "note": "one fc_step captured in a CUDA graph, replayed"}
+        del cg
+    except Exception as exc:  # capture needs a driver that supports it
+        graph = {"unavailable": str(exc).splitlines()[0][:120]}
+
     e2e = None
     if args.e2e_steps > 0:
         host = torch.empty(W * N, dtype=torch.float16, pin_memory=True)
@@ -588,6 +617,7 @@ def run_gpu(args, wl, rank, world, local):
                               "select_update_ms": round(rest_ms, 5)},
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "graph": graph,
             "gpu_launches": 3 * K,
             "clocks": clocks,
         }
