@@ -617,3 +617,56 @@ def test_pipeline_leaves_its_counters_at_zero(name):
     eng.step_layer_groups(g, groups)
     torch.cuda.synchronize()
     assert not _counter_words(eng.workspace, eng.N, eng.chunk).any()
+
+
+def _fuzz_case(i):
+    """Seeded random layout: worker count, layer sizes (with tiny layers),
+    chunk, keep fraction, and per-layer pointer offsets that are either the
+    same for every worker (staged, shifted) or differ (register kernel)."""
+    rng = np.random.default_rng(1000 + i)
+    W = int(rng.choice([4, 8, 16, 4, 8, 16, 4, 8, 16, 3, 5, 32]))
+    L = int(rng.integers(1, 9))
+    sizes = [int(x) for x in np.exp(rng.uniform(0, np.log(60000), L)).astype(int) + 1]
+    if rng.random() < 0.3:                     # a run of tiny layers
+        pos = int(rng.integers(0, L + 1))
+        sizes[pos:pos] = [int(x) for x in rng.integers(1, 9, int(rng.integers(2, 12)))]
+    if rng.random() < 0.85:                    # N % 8 == 0, as the staged kernel needs
+        sizes[-1] += (-sum(sizes)) % 8
+    chunk = int(rng.choice([256, 512, 1024, 2048, 4096, 300, 777]))
+    keep = int(rng.integers(1, 101))
+    mode = rng.choice(["fresh", "uniform", "uniform", "skewed"])
+    shifts = rng.integers(0, 8, len(sizes)) * 2
+    return W, sizes, chunk, keep, str(mode), [int(x) for x in shifts]
+
+
+@pytest.mark.parametrize("i", range(32))
+def test_fuzzed_layouts_match_the_oracle(i):
+    W, sizes, chunk, keep, mode, shifts = _fuzz_case(i)
+    wl = workload.custom(W=W, sizes=sizes, chunk=chunk, keep_percent=keep,
+                         config_id=300 + i, steps=2, loss_scale=256.0)
+
+    def to_dev(g_np):
+        if mode == "fresh":
+            return dev_grads(g_np)
+        out = []
+        for w, row in enumerate(g_np):
+            r = []
+            for l, g in enumerate(row):
+                sh = shifts[l] if mode == "uniform" else (shifts[l] + 2 * w) % 16
+                buf = torch.empty(g.size + 8, dtype=torch.float16, device="cuda")
+                view = buf[sh // 2: sh // 2 + g.size]
+                view.copy_(torch.from_numpy(g))
+                r.append(view)
+            out.append(r)
+        return out
+
+    kinds = set()
+    run = GpuRun(wl, "pipeline")
+    st = oracle.State(workload.initial_weights(wl))
+    for s in range(2):
+        g_np = workload.all_grads(wl, s)
+        g_dev = to_dev(g_np)
+        kinds.add(fc.fc_step_reduce_kernel(g_dev, wl.chunk))
+        run.step(g_dev)
+        oracle_step(g_np, st, wl, run.snapshot())
+    assert len(kinds) == 1
