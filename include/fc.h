@@ -40,8 +40,10 @@
  *
  * Conventions for every call:
  *  - Device pointers are CUDA device (or managed) memory owned by the caller;
- *    host pointers are marked "host".  The library allocates nothing and
- *    keeps no state between calls except the thread-local error message.
+ *    host pointers are marked "host".  The library allocates nothing at run
+ *    time.  Its state between calls is the thread-local error message,
+ *    launch sizes cached per kernel and device, and the scratch array built
+ *    into the library for fc_step_noalloc.
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *    are asynchronous and stream-ordered; a returned FC_OK means the
  *    arguments were valid and the kernels were launched, not that they
@@ -50,8 +52,9 @@
  *    cached the launch configuration).  Kernels run on the device that owns
  *    the call's main device buffer (the output for most calls).
  *  - fp32 arrays and fp16 outputs must be 16-byte aligned; fp16 gradient
- *    inputs must be 2-byte aligned (16-byte aligned ones take the vector
- *    path).  Otherwise FC_ERR_ALIGNMENT.
+ *    inputs must be 2-byte aligned.  Otherwise FC_ERR_ALIGNMENT.  Which
+ *    phase-1 kernel a layout of gradients gets (and so its speed, never its
+ *    result) depends on their alignment: fc_step_reduce_kernel says which.
  *  - Aliasing: only the pairs stated per call may alias.
  *  - Inputs are assumed finite (no inf/NaN in the gradients).
  *  - On error nothing is launched and fc_last_error() describes the cause.
