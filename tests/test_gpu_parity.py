@@ -670,3 +670,58 @@ def test_fuzzed_layouts_match_the_oracle(i):
         run.step(g_dev)
         oracle_step(g_np, st, wl, run.snapshot())
     assert len(kinds) == 1
+
+
+_GUARD_BYTES = 512
+_GUARD_FILL = {torch.float32: (torch.int32, 0x7FA5A5A5), torch.int32: (torch.int32, 0x7FA5A5A5),
+               torch.float16: (torch.int16, 0x7DA5), torch.uint8: (torch.uint8, 0xA5)}
+
+
+def _guard(run):
+    """Moves every device buffer of a GpuRun into the middle of a larger
+    tensor whose margins (512 bytes each side) hold a sentinel pattern;
+    returns the bases and their original contents."""
+    saved = []
+    names = ["weights", "residual", "velocity", "a", "w16", "norms", "idx", "mask", "packed",
+             "packed16", "threshold", "ws", "fused"]
+    inplace_a = run.a is run.residual
+    for name in names:
+        t = getattr(run, name, None)
+        if t is None or (name == "a" and inplace_a):
+            continue
+        g = _GUARD_BYTES // t.element_size()
+        base = torch.empty(t.numel() + 2 * g, dtype=t.dtype, device=t.device)
+        itype, pat = _GUARD_FILL[t.dtype]
+        base.view(itype).fill_(pat if itype != torch.int16 else pat - 65536 * (pat > 32767))
+        view = base[g: g + t.numel()]
+        view.copy_(t)
+        setattr(run, name, view)
+        saved.append((name, base, g, t.numel(), base.clone()))
+    if inplace_a:
+        run.a = run.residual
+    return saved
+
+
+@pytest.mark.parametrize("case", [
+    dict(W=16, sizes=[4096, 808, 8, 6000], chunk=256, keep_percent=25),      # aligned staged
+    dict(W=16, sizes=[1001, 64, 3333, 2, 700, 5000 + 4], chunk=512, keep_percent=30),  # shifted
+    dict(W=5, sizes=[1001, 64, 3333], chunk=300, keep_percent=20),            # register
+    dict(W=3, sizes=[1234, 7], chunk=100, keep_percent=50),                   # N % 8 != 0
+], ids=["aligned", "shifted", "register", "ragged"])
+@pytest.mark.parametrize("path", ["pipeline", "separate"])
+def test_no_call_writes_outside_its_buffers(case, path):
+    """Guard margins around every output, state and workspace buffer stay
+    bit-for-bit untouched over two steps (the stand-in for a memory checker,
+    which is not available on the test machines)."""
+    wl = workload.custom(config_id=400, steps=2, **case)
+    run = GpuRun(wl, path)
+    saved = _guard(run)
+    st = oracle.State(workload.initial_weights(wl))
+    for s in range(2):
+        g_np = workload.all_grads(wl, s)
+        run.step(dev_grads(g_np))
+        oracle_step(g_np, st, wl, run.snapshot())
+    torch.cuda.synchronize()
+    for name, base, g, n, orig in saved:
+        assert torch.equal(base[:g].view(torch.uint8), orig[:g].view(torch.uint8)), name + " head"
+        assert torch.equal(base[g + n:].view(torch.uint8), orig[g + n:].view(torch.uint8)), name + " tail"
