@@ -119,17 +119,55 @@ def oracle_elems_for(wl, seconds):
 
 
 def cpu_baseline(wl, seconds):
+    """Times one oracle step on a sample of the workload; also returns what
+    the parity check needs (the sample, its gradients, the oracle's state
+    after the step and the step's outputs)."""
     import oracle
     m = oracle_elems_for(wl, seconds)
     ws = sample_workload(wl, m)
     g = workload.all_grads(ws, 0)
     st = oracle.State(workload.initial_weights(ws))
-    t = oracle_step_time(ws, g, st)
+    t0 = time.perf_counter()
+    out = oracle.step(g, st, ws.loss_scale, ws.chunk, ws.keep_percent, 100, ws.lr, ws.momentum)
+    t = time.perf_counter() - t0
     gbs = ws.W * ws.N * 2 / t / 1e9
-    return {"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
-            "sample": "one step of the oracle (pack, tree reduce, norms, select, update) on "
-                      "the first %d of %d fused elements of every worker (%.1f%%), %.2f s"
-                      % (ws.N, wl.N, 100.0 * ws.N / wl.N, t)}
+    return ({"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+             "sample": "one step of the oracle (pack, tree reduce, norms, select, update) on "
+                       "the first %d of %d fused elements of every worker (%.1f%%), %.2f s"
+                       % (ws.N, wl.N, 100.0 * ws.N / wl.N, t)},
+            (ws, g, st, out))
+
+
+def parity_check(ws, g, st, out, dev):
+    """One fresh GPU step on the oracle's own inputs, compared with it: the
+    kept indices exactly, residual, velocity and weights bit for bit, the
+    threshold within the 1e-6 band."""
+    import torch
+    from gradient_aggregation_gb300 import fc
+    eng = fc.Engine(ws.sizes, ws.W, ws.chunk, ws.keep_percent, 100, ws.loss_scale, ws.lr,
+                    ws.momentum, torch.from_numpy(workload.initial_weights(ws)).to(dev))
+    gd = [[torch.from_numpy(x).to(dev) for x in row] for row in g]
+    eng.step(gd)
+    torch.cuda.synchronize()
+
+    def same(t, ref):
+        return bool(np.array_equal(t.cpu().numpy().view(np.uint32), ref.view(np.uint32)))
+
+    idx_same = bool(np.array_equal(eng.idx.cpu().numpy(), out["idx"]))
+    thr, thr_ref = float(eng.threshold.cpu()[0]), float(out["threshold"])
+    res = {"checked": "one step of the bench's sample (%d elements x %d workers) against "
+                      "the oracle" % (ws.N, ws.W),
+           "kept_indices_equal": idx_same,
+           "residual_bits_equal": same(eng.residual, st.residual),
+           "velocity_bits_equal": same(eng.velocity, st.velocity),
+           "weights_bits_equal": same(eng.weights, st.weights),
+           "threshold_rel_diff": abs(thr - thr_ref) / max(abs(thr_ref), 1e-30)}
+    ok = idx_same and res["residual_bits_equal"] and res["velocity_bits_equal"] and \
+        res["weights_bits_equal"] and res["threshold_rel_diff"] <= 1e-6
+    res["verdict"] = "pass" if ok else "fail"
+    del eng, gd
+    torch.cuda.empty_cache()
+    return res
 
 
 def run_reference(args, wl, rank):
@@ -590,8 +628,11 @@ def run_gpu(args, wl, rank, world, local):
         del host, stage
 
     cpu = None
+    parity = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        cpu = cpu_baseline(wl, args.cpu_seconds)
+        cpu, sample = cpu_baseline(wl, args.cpu_seconds)
+        parity = parity_check(*sample, dev)
+        del sample
 
     if rank == 0:
         line = {
@@ -616,6 +657,7 @@ def run_gpu(args, wl, rank, world, local):
                               "frac": round(step_alg / (ms_per_step / 1e3) / 1e9 / peak, 4),
                               "select_update_ms": round(rest_ms, 5)},
             "cpu_baseline": cpu,
+            "parity": parity,
             "e2e": e2e,
             "graph": graph,
             "gpu_launches": 3 * K,
