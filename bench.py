@@ -118,6 +118,22 @@ def oracle_elems_for(wl, seconds):
     return max(1024, min(wl.N, int(m * seconds / max(t, 1e-6))))
 
 
+def host_description():
+    """The machine the CPU baseline ran on: architecture, CPU count and,
+    where the system reports one, the CPU model."""
+    import platform
+    model = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                model = line.split(":", 1)[1].strip()
+                break
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return {"machine": platform.machine(), "cpus": os.cpu_count(), "model": model}
+
+
 def cpu_baseline(wl, seconds):
     """Times one oracle step on a sample of the workload; also returns what
     the parity check needs (the sample, its gradients, the oracle's state
@@ -132,6 +148,7 @@ def cpu_baseline(wl, seconds):
     t = time.perf_counter() - t0
     gbs = ws.W * ws.N * 2 / t / 1e9
     return ({"value": round(gbs, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+             "host": host_description(),
              "sample": "one step of the oracle (pack, tree reduce, norms, select, update) on "
                        "the first %d of %d fused elements of every worker (%.1f%%), %.2f s"
                        % (ws.N, wl.N, 100.0 * ws.N / wl.N, t)},
