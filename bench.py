@@ -212,7 +212,8 @@ def run_reference(args, wl, rank):
             "data": "synthetic (seeded Gaussian fp16 gradients, workload-shaped)",
             "config": config_of(wl, {"sample_elements": ws.N}),
             "cpu_baseline": {"value": round(value, 4), "unit": UNIT, "cores": 1,
-                             "kind": "oracle", "sample": sample},
+                             "kind": "oracle", "sample": sample,
+                             "host": host_description()},
             "e2e": {"value": round(value, 4), "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
