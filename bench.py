@@ -481,8 +481,12 @@ def run_gpu(args, wl, rank, world, local):
     # place over the CPU-GPU link, so the reduction consumes the gradients
     # as they arrive (the transfer and the reduction overlap).
     # the same step captured once in a CUDA graph and replayed: no host work
-    # per step (the library's calls are capture-safe)
-    graph = None
+    # per step (the library's calls are capture-safe).  Every rank reaches
+    # the same collectives whether or not its capture worked.
+    graph, graph_err, gt_local = None, None, float("inf")
+    KG = min(K, 1000)
+    torch.cuda.synchronize()
+    barrier()
     try:
         gs = torch.cuda.Stream(device=dev)
         gs.wait_stream(s)
@@ -492,22 +496,24 @@ def run_gpu(args, wl, rank, world, local):
         with torch.cuda.stream(gs):
             for _ in range(max(3, warmup)):
                 cg.replay()
-            KG = min(K, 1000)
             g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             torch.cuda.synchronize()
-            barrier()
             g0.record(gs)
             for _ in range(KG):
                 cg.replay()
             g1.record(gs)
         torch.cuda.synchronize()
-        gt = max_t(g0.elapsed_time(g1) / 1e3)
+        gt_local = g0.elapsed_time(g1) / 1e3
+        del cg
+    except Exception as exc:  # capture needs a driver that supports it
+        graph_err = str(exc).splitlines()[0][:120] if str(exc) else type(exc).__name__
+    gt = max_t(gt_local)
+    if graph_err is None and gt != float("inf"):
         graph = {"value": round(replica_value(world, W * N * 2, KG, gt), 3), "unit": UNIT,
                  "ms_per_step": round(gt * 1e3 / KG, 5), "steps": KG,
                  "note": "one fc_step captured in a CUDA graph, replayed"}
-        del cg
-    except Exception as exc:  # capture needs a driver that supports it
-        graph = {"unavailable": str(exc).splitlines()[0][:120]}
+    else:
+        graph = {"unavailable": graph_err or "capture failed on another rank"}
 
     e2e = None
     if args.e2e_steps > 0:
