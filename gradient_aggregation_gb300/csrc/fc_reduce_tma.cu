@@ -326,7 +326,27 @@ __global__ void __launch_bounds__(kThreads, 1)
                             },
                             a);
                     } else {
-                        // at a layer boundary (or unstaged): from global memory
+                        // at a layer boundary (or unstaged): from global memory.
+                        // Within two layers: two pointers per worker, all 8
+                        // elements of a worker loaded together.
+                        int la = pc.z;
+                        while (tab.off[la + 1] <= f) ++la;
+                        int lb = la;
+                        while (tab.off[lb + 1] <= f + 7) ++lb;
+                        if (lb - la <= 1) {
+                            const int64_t ja = f - tab.off[la], jb = f - tab.off[lb];
+                            const int split = (int)(tab.off[la + 1] - f < 8 ? tab.off[la + 1] - f : 8);
+                            tree_sum<WT, MAXH, 8>(
+                                W,
+                                [&](int w, float(&x)[8]) {
+                                    const __half *pa = tab.ptr[w * L + la] + ja;
+                                    const __half *pb = tab.ptr[w * L + lb] + jb;
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e)
+                                        x[e] = ld_half_as_float(e < split ? pa + e : pb + e);
+                                },
+                                a);
+                        } else {
                         int l = pc.z;
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
@@ -340,6 +360,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 },
                                 s1);
                             a[e] = s1[0];
+                        }
                         }
                     }
                 }
