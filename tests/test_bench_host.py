@@ -109,3 +109,18 @@ def test_group_major_layout_places_each_group_in_one_block():
     assert None not in buf
     for (a, b), (lo, hi) in zip(groups, span):      # a group's block holds its layers only
         assert {buf[i][1] for i in range(lo, hi)} == set(range(a, b))
+
+
+def test_cpu_baseline_takes_the_median_of_several_oracle_steps():
+    import numpy as np
+    import oracle
+    from gradient_aggregation_gb300 import workload
+    wl = workload.get("tiny")
+    line, (ws, g, first, out) = bench.cpu_baseline(wl, 0.3)
+    assert line["kind"] == "oracle" and line["cores"] == 1 and line["value"] > 0
+    assert "median of" in line["sample"] and line["host"]["cpus"] >= 1
+    # the parity material is the state after exactly one step
+    st = oracle.State(workload.initial_weights(ws))
+    ref = oracle.step(g, st, ws.loss_scale, ws.chunk, ws.keep_percent, 100, ws.lr, ws.momentum)
+    assert np.array_equal(ref["idx"], out["idx"])
+    assert np.array_equal(st.weights.view(np.uint32), first.weights.view(np.uint32))
