@@ -725,3 +725,48 @@ def test_no_call_writes_outside_its_buffers(case, path):
     for name, base, g, n, orig in saved:
         assert torch.equal(base[:g].view(torch.uint8), orig[:g].view(torch.uint8)), name + " head"
         assert torch.equal(base[g + n:].view(torch.uint8), orig[g + n:].view(torch.uint8)), name + " tail"
+
+
+def test_engines_on_several_host_threads_match_sequential_runs():
+    """Four host threads, each stepping its own engine on its own stream
+    (staged shifted, staged aligned, register and large-table layouts), give
+    the bits of the same steps run one after another: the host-side caches
+    and the thread-local tables are safe to use concurrently."""
+    import threading
+    cases = [dict(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512, keep_percent=30),
+             dict(W=8, sizes=[4096, 808, 8, 6000], chunk=256, keep_percent=25),
+             dict(W=5, sizes=[1001, 64, 3333], chunk=300, keep_percent=20),
+             dict(W=16, sizes=[97 + 8 * i for i in range(40)], chunk=256, keep_percent=10)]
+    wls = [workload.custom(config_id=420 + i, steps=3, **c) for i, c in enumerate(cases)]
+    grads = [[dev_grads(workload.all_grads(wl, s)) for s in range(3)] for wl in wls]
+
+    def run(i, engine, stream):
+        with torch.cuda.stream(stream):
+            for s in range(3):
+                engine.step(grads[i][s], stream)
+        stream.synchronize()
+
+    seq = [_engine(wl) for wl in wls]
+    for i, e in enumerate(seq):
+        run(i, e, torch.cuda.Stream())
+    par = [_engine(wl) for wl in wls]
+    streams = [torch.cuda.Stream() for _ in wls]
+    errors = []
+
+    def worker(i):
+        try:
+            run(i, par[i], streams[i])
+        except Exception as exc:  # reported below
+            errors.append(exc)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(wls))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    torch.cuda.synchronize()
+    for a, b in zip(seq, par):
+        wa, wb = _engine_bits(a), _engine_bits(b)
+        for k in wa:
+            assert bits_equal(wa[k], wb[k]), k
