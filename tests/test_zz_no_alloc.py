@@ -34,13 +34,16 @@ def _noalloc_step(run, grads):
                        run.packed16, run.send_scale)
 
 
-@pytest.mark.parametrize("name", ["tiny", "custom"])
+@pytest.mark.parametrize("name", ["tiny", "custom", "shifted"])
 def test_noalloc_matches_workspace_pipeline_on_two_calls(name):
     if name == "tiny":
         wl = workload.get("tiny")
-    else:
+    elif name == "custom":
         wl = workload.custom(W=7, sizes=[5000, 33, 12000], chunk=1000, keep_percent=30,
                              config_id=170, steps=2)
+    else:                             # the staged kernel's shifted layout
+        wl = workload.custom(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512,
+                             keep_percent=30, config_id=171, steps=2)
     ref = GpuRun(wl, "pipeline")      # fc_step with a caller workspace
     new = GpuRun(wl, "pipeline")      # same buffers, stepped by fc_step_noalloc
     for step in range(2):
