@@ -711,8 +711,8 @@ def _guard(run):
 @pytest.mark.parametrize("path", ["pipeline", "separate"])
 def test_no_call_writes_outside_its_buffers(case, path):
     """Guard margins around every output, state and workspace buffer stay
-    bit-for-bit untouched over two steps (the stand-in for a memory checker,
-    which is not available on the test machines)."""
+    bit-for-bit untouched over two steps: a memory checker's out-of-bounds
+    write detection, done by the test itself."""
     wl = workload.custom(config_id=400, steps=2, **case)
     run = GpuRun(wl, path)
     saved = _guard(run)
