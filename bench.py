@@ -41,7 +41,6 @@ from gradient_aggregation_gb300 import workload  # noqa: E402
 
 METRIC = "worker-gradient GB/s aggregated (1xGB300) and % of HBM roofline vs CPU oracle"
 UNIT = "GB/s"
-TILE = 2048  # elements per tile of the kernels (FC_TILE)
 
 
 def parse():
@@ -360,6 +359,46 @@ def traffic_from_profile(src_hash, wl):
         return None
 
 
+MIN_PHASE1 = 20   # phase-1 launches timed at least, at any --steps
+
+
+def phase1_every(steps: int) -> int:
+    """Time phase 1 on every n-th step: one in eight on long runs, more often
+    on short ones so that at least MIN_PHASE1 launches are timed."""
+    return max(1, min(8, steps // MIN_PHASE1))
+
+
+def units_of(N: int, chunk: int) -> int:
+    """256-element units of the fused vector (none straddles a chunk)."""
+    C = -(-N // chunk)
+    U = -(-chunk // 256)
+    return (C - 1) * U + -(-(N - (C - 1) * chunk) // 256)
+
+
+def step_algorithmic_bytes(wl, k: int) -> dict:
+    """Algorithmic bytes of one pipeline step with `a` formed in place in the
+    residual buffer, per kernel, and the plain count N*(2W+32):
+      phase 1: the W workers' fp16 gradients, the residual read, `a`
+               written, one fp32 sum of squares per 256-element unit;
+      phase 2: the unit sums read; norms, mask, kept-slot map and idx
+               written;
+      phase 3: velocity and weights read and written for every element;
+               for kept elements `a` read, the residual zeroed and the
+               packed fp32 send buffer written.  In place, unkept elements'
+               `a` is already their new residual: neither read nor written.
+    The plain count also reads `a` and writes the residual for every
+    element (8N more) and leaves out the unit sums and the selection."""
+    W, N = wl.W, wl.N
+    C = -(-N // wl.chunk)
+    units = units_of(N, wl.chunk)
+    kept_el = min(N, k * wl.chunk)       # at most; a kept short last chunk has fewer
+    phase1 = 2 * W * N + 4 * N + 4 * N + 4 * units
+    phase2 = 4 * units + 4 * C + C + 4 * C + 4 * k
+    phase3 = 16 * N + 8 * kept_el + 4 * k * wl.chunk   # + the zero-padded send slots
+    return {"phase1": phase1, "phase2": phase2, "phase3": phase3,
+            "step": phase1 + phase2 + phase3, "survey": N * (2 * W + 32)}
+
+
 def max_over_ranks(x: float, device=None) -> float:
     """The largest of every rank's x (identity without a process group)."""
     import torch
@@ -415,17 +454,12 @@ def run_gpu(args, wl, rank, world, local):
         phases[1]()
         phases[2]()
 
-    torch.cuda.synchronize()
-    warmup = max(3, args.warmup)   # at least three untimed steps
-    for _ in range(warmup):
-        step_phased()
-    torch.cuda.synchronize()
-
     K = args.steps
-    # Phase-1 events bracket the reduction kernel on every EVERY-th step only:
-    # an event between two kernels stops the next one from being scheduled
-    # early (programmatic dependent launch), so most steps run without one.
-    EVERY = 8
+    # Phase-1 events bracket the reduction kernel on every EVERY-th step, so
+    # that at least MIN_PHASE1 launches are timed at any step count: an event
+    # between two kernels stops the next one from being scheduled early
+    # (programmatic dependent launch), so long runs time one step in eight.
+    EVERY = phase1_every(K)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            if i % EVERY == 0 else None for i in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -439,8 +473,13 @@ def run_gpu(args, wl, rank, world, local):
     sampler = ClockSampler(uuid)
     sampler.start()
     time.sleep(0.35)
-    barrier()
+    # warm-up directly before the timed steps: no idle gap in which the
+    # clocks could drop
     torch.cuda.synchronize()
+    barrier()
+    warmup = max(3, args.warmup)   # at least three untimed steps
+    for _ in range(warmup):
+        step_phased()
     t_wall0 = time.time()
     start.record(s)
     for i in range(K):
@@ -462,9 +501,31 @@ def run_gpu(args, wl, rank, world, local):
 
     # roofline of the dominant kernel (phase 1: tree reduce + norm partials)
     C = -(-N // wl.chunk)
-    P = -(-wl.chunk // TILE)
-    k_alg = W * N * 2 + 4 * N + 4 * N + 8 * C * P
+    alg = step_algorithmic_bytes(wl, eng.k)
+    k_alg = alg["phase1"]
     k_ms = statistics.mean(reduce_ms)
+
+    # the same phase-1 kernel launched back to back on its own (out of place,
+    # so the engine's state is untouched), at least MIN_PHASE1 launches
+    iso = None
+    try:
+        a_tmp = torch.empty(N, dtype=torch.float32, device=dev)
+        for _ in range(3):
+            fc.fc_step_reduce(table, wl.loss_scale, wl.chunk, eng.residual, a_tmp,
+                              eng.workspace, s)
+        i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        KI = max(MIN_PHASE1, min(K, 200))
+        i0.record(s)
+        for _ in range(KI):
+            fc.fc_step_reduce(table, wl.loss_scale, wl.chunk, eng.residual, a_tmp,
+                              eng.workspace, s)
+        i1.record(s)
+        torch.cuda.synchronize()
+        iso_ms = i0.elapsed_time(i1) / KI
+        del a_tmp
+        iso = {"avg_launch_ms": round(iso_ms, 5), "launches": KI}
+    except Exception as exc:
+        iso = {"unavailable": str(exc).splitlines()[0][:120] if str(exc) else type(exc).__name__}
     peaks = {}
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
@@ -479,9 +540,10 @@ def run_gpu(args, wl, rank, world, local):
 
     # the rest of the step: select + update, measured as step minus phase 1
     rest_ms = ms_per_step - k_ms
-    kept_frac = eng.k * wl.chunk / N
-    update_alg = N * (16 + 8 * min(1.0, kept_frac))    # in place: v,w r/w; kept: a, r, packed
-    step_alg = k_alg + update_alg
+    step_alg = alg["step"]
+    if iso and "avg_launch_ms" in iso:
+        iso["achieved"] = round(k_alg / (iso["avg_launch_ms"] / 1e3) / 1e9, 1)
+        iso["frac"] = round(iso["achieved"] / peak, 4)
 
     # End to end through the public API: every step moves all workers'
     # gradients from pinned host memory to the GPU and reads the step's result
@@ -741,13 +803,25 @@ def run_gpu(args, wl, rank, world, local):
                       % (step_bytes / 1e9, 12 * N / 1e9)}),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
-                         "traffic": traffic, "kernel": "phase 1 of fc_step (%s)" % phase1_kernel(wl, table),
+                         "traffic": traffic,
+                         "traffic_source": ("dram__bytes_read.sum + dram__bytes_write.sum of "
+                                            "one launch, from the committed ncu summary "
+                                            "profiles/k_reduce_%s.md taken on this kernel "
+                                            "source (not measured in this run)" % wl.name)
+                                           if traffic is not None else None,
+                         "kernel": "phase 1 of fc_step (%s)" % phase1_kernel(wl, table),
                          "algorithmic_bytes_per_launch": k_alg,
-                         "avg_launch_ms": round(k_ms, 5), "peak_source": peak_src + " hbm_gbs",
-                         "timed_launches": len(reduce_ms)},
+                         "avg_launch_ms": round(k_ms, 5),
+                         "median_launch_ms": round(statistics.median(reduce_ms), 5),
+                         "peak_source": peak_src + " hbm_gbs",
+                         "timed_launches": len(reduce_ms),
+                         "isolated": iso},
             "step_roofline": {"algorithmic_bytes_per_step": int(step_alg),
+                              "survey_count_bytes_per_step": int(alg["survey"]),
                               "achieved_gbs": round(step_alg / (ms_per_step / 1e3) / 1e9, 1),
                               "frac": round(step_alg / (ms_per_step / 1e3) / 1e9 / peak, 4),
+                              "survey_count_frac": round(alg["survey"] / (ms_per_step / 1e3)
+                                                         / 1e9 / peak, 4),
                               "select_update_ms": round(rest_ms, 5)},
             "cpu_baseline": cpu,
             "parity": parity,

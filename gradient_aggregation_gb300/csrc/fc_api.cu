@@ -48,28 +48,6 @@ fc_status cuda_fail(cudaError_t e, const char *what)
 
 bool aligned(const void *p, uintptr_t a) { return ((uintptr_t)p & (a - 1)) == 0; }
 
-// Makes the device that owns `ptr` (a device pointer argument of the call)
-// current.  Only queries that are legal while a stream is being captured
-// into a CUDA graph are used.
-fc_status bind_device(void *stream, const void *ptr)
-{
-    (void)stream;
-    (void)cudaGetLastError();  // clear a stale error of this runtime
-    cudaPointerAttributes at;
-    cudaError_t e = cudaPointerGetAttributes(&at, ptr);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
-    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
-        return fail(FC_ERR_INVALID_ARG, "pointer %p is not device memory", ptr);
-    int cur = -1;
-    e = cudaGetDevice(&cur);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
-    if (cur != at.device) {
-        e = cudaSetDevice(at.device);
-        if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
-    }
-    return FC_OK;
-}
-
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 TileGeom geom(int64_t N, int64_t cs)
@@ -95,9 +73,10 @@ UnitGeom ugeom(int64_t N, int64_t cs)
 
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
-// Workspace of the pipeline: unit sums (float [units]), the selection's
-// count of finished blocks (zero between calls) and the kept-slot map
-// (int32 [C]).
+// Workspace of the pipeline: unit sums (float [units]), a 256-byte block of
+// words (0: the selection's count of finished blocks, zero between calls;
+// 1: the staged reduction's failure word, zero between calls; 2: the last
+// step's outcome, 0 = applied) and the kept-slot map (int32 [C]).
 struct WsLayout {
     size_t partials, counters, slot, total;
 };
@@ -192,7 +171,7 @@ extern "C" {
 
 const char *fc_last_error(void) { return g_err; }
 
-int32_t fc_version(void) { return 100; }
+int32_t fc_version(void) { return 200; }
 
 int64_t fc_num_chunks(int64_t N, int64_t chunk)
 {
@@ -239,7 +218,8 @@ fc_status fc_fuse_pack(const void *const *grads, int32_t W, int32_t L,
     if (!fused) return fail(FC_ERR_INVALID_ARG, "fused is NULL");
     if (!aligned(fused, 16)) return fail(FC_ERR_ALIGNMENT, "fused is not 16-byte aligned");
     if (offsets) TRY(fc_layout(L, sizes, offsets, nullptr));
-    TRY(bind_device(stream, fused));
+    DeviceScope scope;
+    TRY(scope.bind(fused));
     cudaError_t e;
     if (fits_small(W, L)) {
         TableS tab;
@@ -270,7 +250,8 @@ fc_status fc_reduce_ordered(const void *fused, int32_t W, int64_t N,
     if (!aligned(fused, 2)) return fail(FC_ERR_ALIGNMENT, "fused is not 2-byte aligned");
     TRY(check_f32(residual_in, "residual_in", true));
     TRY(check_f32(out, "out", false));
-    TRY(bind_device(stream, out));
+    DeviceScope scope;
+    TRY(scope.bind(out));
     const float u = (float)(1.0 / ((double)loss_scale * (double)W));
     const UnitGeom G = ugeom(N, N);  // one chunk: no norms here
     const int64_t sizes[1] = {N};
@@ -309,10 +290,17 @@ fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
     if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
     TRY(check_f32(a, "a", false));
     TRY(check_f32(norms, "norms", false));
-    TRY(bind_device(stream, a));
+    DeviceScope scope;
+    TRY(scope.bind(a));
     cudaError_t e = launch_norms(a, ugeom(N, chunk), norms, (cudaStream_t)stream);
     if (e != cudaSuccess) return cuda_fail(e, "chunk_norms launch");
     return ok();
+}
+
+size_t fc_chunk_select_workspace(int64_t C)
+{
+    (void)C;  // the selection's scratch lives in one block's shared memory
+    return 0;
 }
 
 static fc_status check_select_args(int64_t C, int64_t k, const int32_t *idx,
@@ -346,7 +334,8 @@ fc_status fc_chunk_select(const float *norms, int64_t C, int64_t k,
         if (chunk < 1 || N < 1 || ceil_div(N, chunk) != C)
             return fail(FC_ERR_INVALID_ARG, "N and chunk do not give C chunks");
     }
-    TRY(bind_device(stream, norms));
+    DeviceScope scope;
+    TRY(scope.bind(norms));
     UnitGeom G;
     G.N = N;
     G.cs = chunk;
@@ -392,7 +381,8 @@ fc_status fc_residual_sgd_update(const float *a, const uint8_t *mask,
     TraceRange trace("fc_residual_sgd_update");
     TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
                           weights, weights_fp16));
-    TRY(bind_device(stream, a));
+    DeviceScope scope;
+    TRY(scope.bind(a));
     const TileGeom G = geom(N, chunk);
     const int64_t tiles = ceil_div(N, chunk) * G.P;
     cudaError_t e = launch_update(G, tiles, a, mask, nullptr, nullptr, nullptr, 1.f, lr,
@@ -457,7 +447,8 @@ static fc_status reduce_span(const char *name, const void *const *grads, int32_t
     TRY(check_f32(residual, "residual", true));
     TRY(check_f32(a, "a", false));
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
-    TRY(bind_device(stream, a));
+    DeviceScope scope;
+    TRY(scope.bind(a));
     const float u = (float)(1.0 / ((double)loss_scale * (double)W));
     const UnitGeom G = ugeom(N, chunk);
     const WsLayout wl = ws_layout(N, chunk);
@@ -573,13 +564,15 @@ fc_status fc_step_select(int64_t N, int64_t chunk, int64_t k, float *norms,
     TRY(check_select_args(C, k, idx, mask, threshold));
     TRY(check_f32(norms, "norms", false));
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
-    TRY(bind_device(stream, norms));
+    DeviceScope scope;
+    TRY(scope.bind(norms));
     const WsLayout wl = ws_layout(N, chunk);
     const float *partials = (const float *)((const char *)workspace + wl.partials);
     unsigned *done = (unsigned *)((char *)workspace + wl.counters);
     int32_t *slot = (int32_t *)((char *)workspace + wl.slot);
     cudaError_t e = launch_select(ugeom(N, chunk), partials, done, norms, k, idx,
-                                  mask, slot, threshold, (cudaStream_t)stream, done + 1);
+                                  mask, slot, threshold, (cudaStream_t)stream, done + 1,
+                                  done + 2);
     if (e != cudaSuccess) return cuda_fail(e, "step_select launch");
     return ok();
 }
@@ -598,15 +591,18 @@ fc_status fc_step_update(const float *a, int64_t N, int64_t chunk, float lr,
     TRY(check_f32(packed_fp16, "packed_fp16", true));
     if (!isfinite(send_scale)) return fail(FC_ERR_INVALID_ARG, "send_scale must be finite");
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
-    TRY(bind_device(stream, a));
+    DeviceScope scope;
+    TRY(scope.bind(a));
     const TileGeom G = geom(N, chunk);
     const int64_t C = ceil_div(N, chunk);
-    const int32_t *slot = (const int32_t *)((char *)workspace + ws_layout(N, chunk).slot);
+    const WsLayout wl = ws_layout(N, chunk);
+    const int32_t *slot = (const int32_t *)((char *)workspace + wl.slot);
+    const unsigned *status = (const unsigned *)((char *)workspace + wl.counters) + 2;
     cudaError_t e = launch_update(G, C * G.P, a, mask, slot, packed,
                                   (__half *)packed_fp16, send_scale, lr,
                                   momentum, residual, velocity, weights,
                                   (__half *)weights_fp16, a == residual,
-                                  (cudaStream_t)stream);
+                                  (cudaStream_t)stream, status);
     if (e != cudaSuccess) return cuda_fail(e, "step_update launch");
     return ok();
 }
@@ -622,18 +618,12 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
 {
     TraceRange trace("fc_step");
     int64_t N = 0;
-    TRY(check_sizes(L, sizes, &N));
     // check everything before the first launch so that an error launches
     // nothing
-    TRY(check_table(grads, W, L, sizes));
-    if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
-    TRY(check_select_args(ceil_div(N, chunk), k, idx, mask, threshold));
-    TRY(check_f32(norms, "norms", false));
-    TRY(check_update_args(a, mask, N, chunk, lr, momentum, residual, velocity,
-                          weights, weights_fp16));
-    TRY(check_f32(packed, "packed", true));
-    TRY(check_f32(packed_fp16, "packed_fp16", true));
-    if (!isfinite(send_scale)) return fail(FC_ERR_INVALID_ARG, "send_scale must be finite");
+    TRY(check_step_args(grads, W, L, sizes, loss_scale, chunk, k, lr, momentum, residual, a,
+                        velocity, weights, weights_fp16, norms, idx, mask, packed,
+                        packed_fp16, send_scale, threshold, &N));
+    TRY(check_ws(N, chunk, workspace, workspace_bytes));
     TRY(fc_step_reduce(grads, W, L, sizes, loss_scale, chunk, residual, a,
                        workspace, workspace_bytes, stream));
     TRY(fc_step_select(N, chunk, k, norms, idx, mask, threshold, workspace,
@@ -641,6 +631,28 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
     TRY(fc_step_update(a, N, chunk, lr, momentum, residual, velocity, weights,
                        weights_fp16, mask, packed, packed_fp16, send_scale,
                        workspace, workspace_bytes, stream));
+    return ok();
+}
+
+fc_status fc_step_status(const void *workspace, size_t workspace_bytes, int64_t N,
+                         int64_t chunk, void *stream)
+{
+    TraceRange trace("fc_step_status");
+    if (N < 1 || chunk < 1) return fail(FC_ERR_INVALID_ARG, "N and chunk must be >= 1");
+    TRY(check_ws(N, chunk, const_cast<void *>(workspace), workspace_bytes));
+    DeviceScope scope;
+    TRY(scope.bind(workspace));
+    const unsigned *word =
+        (const unsigned *)((const char *)workspace + ws_layout(N, chunk).counters) + 2;
+    unsigned h = 0;
+    cudaError_t e = cudaMemcpyAsync(&h, word, sizeof(h), cudaMemcpyDeviceToHost,
+                                    (cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemcpyAsync of the step status");
+    e = cudaStreamSynchronize((cudaStream_t)stream);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    if (h != 0u)
+        return fail(FC_ERR_TIMEOUT, "the last step was not applied: a bounded wait of its "
+                                    "staged reduction ran out");
     return ok();
 }
 
@@ -659,6 +671,58 @@ fc_status set_error(fc_status st, const char *msg)
 size_t step_ws_counter_offset(int64_t N, int64_t chunk)
 {
     return ws_layout(N, chunk).counters;
+}
+
+fc_status DeviceScope::bind(const void *ptr)
+{
+    (void)cudaGetLastError();  // clear a stale error of this runtime
+    cudaPointerAttributes at;
+    cudaError_t e = cudaPointerGetAttributes(&at, ptr);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaPointerGetAttributes");
+    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
+        return fail(FC_ERR_INVALID_ARG, "pointer %p is not device memory", ptr);
+    int cur = -1;
+    e = cudaGetDevice(&cur);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (cur != at.device) {
+        e = cudaSetDevice(at.device);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaSetDevice");
+        if (prev_ < 0) prev_ = cur;
+    }
+    dev_ = at.device;
+    return FC_OK;
+}
+
+DeviceScope::~DeviceScope()
+{
+    if (prev_ >= 0) (void)cudaSetDevice(prev_);
+}
+
+fc_status check_step_args(const void *const *grads, int32_t W, int32_t L,
+                          const int64_t *sizes, float loss_scale, int64_t chunk,
+                          int64_t k, float lr, float momentum, const float *residual,
+                          const float *a, const float *velocity, const float *weights,
+                          const void *weights_fp16, const float *norms, const int32_t *idx,
+                          const uint8_t *mask, const float *packed, const void *packed_fp16,
+                          float send_scale, const float *threshold, int64_t *N_out)
+{
+    int64_t N = 0;
+    TRY(check_sizes(L, sizes, &N));
+    TRY(check_table(grads, W, L, sizes));
+    if (chunk < 1) return fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
+    if (!(loss_scale > 0.f) || !isfinite(loss_scale))
+        return fail(FC_ERR_INVALID_ARG, "loss_scale must be finite and > 0");
+    TRY(check_select_args(ceil_div(N, chunk), k, idx, mask, threshold));
+    TRY(check_f32(norms, "norms", false));
+    TRY(check_f32(residual, "residual", true));
+    TRY(check_update_args(a, mask, N, chunk, lr, momentum, const_cast<float *>(residual),
+                          const_cast<float *>(velocity), const_cast<float *>(weights),
+                          const_cast<void *>(weights_fp16)));
+    TRY(check_f32(packed, "packed", true));
+    TRY(check_f32(packed_fp16, "packed_fp16", true));
+    if (!isfinite(send_scale)) return fail(FC_ERR_INVALID_ARG, "send_scale must be finite");
+    *N_out = N;
+    return FC_OK;
 }
 
 }  // namespace fc

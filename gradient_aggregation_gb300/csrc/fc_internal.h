@@ -48,25 +48,58 @@ cudaError_t launch_norms(const float *a, const UnitGeom &G, float *norms,
 // With partials == NULL, norms [C] is the input.  Otherwise the chunk
 // norms are first formed from the unit sums (partials [G.units]) by many
 // blocks and written to norms; `done` (zero on entry, zero on exit) counts
-// finished blocks and the last one selects.  slot may be NULL.
+// finished blocks and the last one selects.  slot may be NULL.  err: the
+// staged reduction's failure word (read and cleared); status: the step's
+// outcome word, written with 0 (applied) or 1 (not applied: a wait ran out).
 cudaError_t launch_select(const UnitGeom &G, const float *partials,
                           unsigned *done, float *norms, int64_t k,
                           int32_t *idx, uint8_t *mask, int32_t *slot,
                           float *threshold, cudaStream_t s,
-                          unsigned *err = nullptr);
+                          unsigned *err = nullptr, unsigned *status = nullptr);
 
 cudaError_t launch_gather(const float *a, int64_t N, int64_t cs, int64_t P,
                           const int32_t *idx, int64_t k, float *packed,
                           __half *packed16, float send_scale, cudaStream_t s);
 
+// status (may be NULL): the step's outcome word written by the selection;
+// when it is non-zero the update writes nothing.
 cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           const uint8_t *mask, const int32_t *slot,
                           float *packed, __half *packed16, float send_scale,
                           float lr, float mu, float *r, float *v, float *w,
-                          __half *w16, bool inplace, cudaStream_t s);
+                          __half *w16, bool inplace, cudaStream_t s,
+                          const unsigned *status = nullptr);
 
 // Sets the calling thread's fc_last_error() message; returns st.
 fc_status set_error(fc_status st, const char *msg);
+
+// Makes the device that owns a pointer argument current for the rest of an
+// entry point, and makes the caller's device current again when the scope
+// ends.  Uses only queries that are legal while a stream is captured.
+class DeviceScope {
+public:
+    DeviceScope() = default;
+    DeviceScope(const DeviceScope &) = delete;
+    DeviceScope &operator=(const DeviceScope &) = delete;
+    ~DeviceScope();
+    // FC_OK, or an error status with fc_last_error() set.
+    fc_status bind(const void *device_ptr);
+    int device() const { return dev_; }
+
+private:
+    int prev_ = -1;  // the caller's device, if it was changed
+    int dev_ = -1;
+};
+
+// Every argument check of fc_step except the workspace; the fused length
+// goes to *N_out.  Queues nothing.
+fc_status check_step_args(const void *const *grads, int32_t W, int32_t L,
+                          const int64_t *sizes, float loss_scale, int64_t chunk,
+                          int64_t k, float lr, float momentum, const float *residual,
+                          const float *a, const float *velocity, const float *weights,
+                          const void *weights_fp16, const float *norms, const int32_t *idx,
+                          const uint8_t *mask, const float *packed, const void *packed_fp16,
+                          float send_scale, const float *threshold, int64_t *N_out);
 
 // Byte offset, inside the pipeline workspace for (N, chunk), of the 256-byte
 // word block that must be zero before a step.

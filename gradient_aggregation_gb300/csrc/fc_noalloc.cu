@@ -5,8 +5,12 @@
 // The array below is a file-scope __device__ variable: every GPU that loads
 // the library holds FC_NOALLOC_WORKSPACE_BYTES of it until the process exits.
 // In host code the name `g_noalloc_ws` is only a host-side stand-in, not a
-// device address, so the device address is looked up once per device with
-// cudaGetSymbolAddress while that device is current, checked, and cached.
+// device address, so the device address is looked up with
+// cudaGetSymbolAddress while the device is current, checked, and cached.
+// The cache entry of a device remembers the identity of the CUDA context it
+// was looked up in: cudaDeviceReset destroys that context (and with it the
+// array's mapping), and the next call, seeing another context, looks the
+// address up again instead of handing the kernels a stale one.
 #include <stdio.h>
 
 #include <mutex>
@@ -19,11 +23,62 @@ namespace {
 __device__ __align__(256) unsigned char g_noalloc_ws[FC_NOALLOC_WORKSPACE_BYTES];
 
 constexpr int kMaxDevices = 64;
+
+struct CacheEntry {
+    void *addr;
+    unsigned long long ctx_id;  // 0: unknown, look the address up every call
+};
+
 std::mutex g_mu;
-void *g_addr[kMaxDevices];
+CacheEntry g_cache[kMaxDevices];
+
+// Driver calls reached through the runtime's entry-point query, so that the
+// library needs no link against the driver library.  Both are plain queries
+// (legal while a stream is being captured).
+using CtxGetCurrentFn = int (*)(void **ctx);
+using CtxGetIdFn = int (*)(void *ctx, unsigned long long *id);
+
+struct DriverQueries {
+    CtxGetCurrentFn get_current = nullptr;
+    CtxGetIdFn get_id = nullptr;
+};
+
+const DriverQueries &driver_queries()
+{
+    static DriverQueries q = [] {
+        DriverQueries d;
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult res;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault,
+                                             &res) == cudaSuccess &&
+            res == cudaDriverEntryPointSuccess)
+            d.get_current = reinterpret_cast<CtxGetCurrentFn>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault,
+                                             &res) == cudaSuccess &&
+            res == cudaDriverEntryPointSuccess)
+            d.get_id = reinterpret_cast<CtxGetIdFn>(fn);
+        return d;
+    }();
+    return q;
+}
+
+// Identity of the calling thread's current CUDA context (unique for the life
+// of the process), or 0 if the driver cannot say.
+unsigned long long current_context_id()
+{
+    const DriverQueries &q = driver_queries();
+    if (!q.get_current || !q.get_id) return 0;
+    void *ctx = nullptr;
+    if (q.get_current(&ctx) != 0 || !ctx) return 0;
+    unsigned long long id = 0;
+    if (q.get_id(ctx, &id) != 0) return 0;
+    return id;
+}
 
 // Device address of the array on device `dev`, which must be current.
-// Looked up on the first call for that device and cached afterwards.
+// Looked up on the first call for that device (and again whenever the
+// device's context has changed since), cached otherwise.
 fc_status noalloc_workspace(int dev, void **out)
 {
     char msg[256];
@@ -31,18 +86,23 @@ fc_status noalloc_workspace(int dev, void **out)
         snprintf(msg, sizeof(msg), "device %d is out of range", dev);
         return fc::set_error(FC_ERR_CUDA, msg);
     }
+    const unsigned long long ctx = current_context_id();
     std::lock_guard<std::mutex> lock(g_mu);
-    if (!g_addr[dev]) {
+    CacheEntry &e = g_cache[dev];
+    if (!e.addr || ctx == 0 || e.ctx_id != ctx) {
         void *p = nullptr;
-        const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_ws);
-        if (e != cudaSuccess || !p) {
+        const cudaError_t err = cudaGetSymbolAddress(&p, g_noalloc_ws);
+        if (err != cudaSuccess || !p) {
+            e.addr = nullptr;
             snprintf(msg, sizeof(msg), "cudaGetSymbolAddress of the built-in scratch: %s",
-                     cudaGetErrorString(e));
+                     cudaGetErrorString(err));
             return fc::set_error(FC_ERR_CUDA, msg);
         }
-        g_addr[dev] = p;
+        e.addr = p;
+        // the lookup may have created the context: ask again
+        e.ctx_id = ctx != 0 ? ctx : current_context_id();
     }
-    *out = g_addr[dev];
+    *out = e.addr;
     return FC_OK;
 }
 
@@ -61,9 +121,11 @@ fc_status fc_step_noalloc(const void *const *grads, int32_t W, int32_t L,
 {
     char msg[256];
     int64_t N = 0;
-    fc_status st = fc_layout(L, sizes, nullptr, &N);
+    // every argument first, so that an invalid call queues nothing
+    fc_status st = fc::check_step_args(grads, W, L, sizes, loss_scale, chunk, k, lr, momentum,
+                                       residual, a, velocity, weights, weights_fp16, norms, idx,
+                                       mask, packed, packed_fp16, send_scale, threshold, &N);
     if (st != FC_OK) return st;
-    if (chunk < 1) return fc::set_error(FC_ERR_INVALID_ARG, "chunk must be >= 1");
     const size_t need = fc_step_workspace_size(N, chunk);
     if (need > (size_t)FC_NOALLOC_WORKSPACE_BYTES) {
         snprintf(msg, sizeof(msg),
@@ -72,29 +134,20 @@ fc_status fc_step_noalloc(const void *const *grads, int32_t W, int32_t L,
                  (long long)N, (long long)chunk, need, (size_t)FC_NOALLOC_WORKSPACE_BYTES);
         return fc::set_error(FC_ERR_LIMIT, msg);
     }
-    if (!a) return fc::set_error(FC_ERR_INVALID_ARG, "a is NULL");
-    // the device that owns the output is the one whose copy of the array is used
-    cudaPointerAttributes at;
-    cudaError_t e = cudaPointerGetAttributes(&at, a);
-    if (e != cudaSuccess) {
-        snprintf(msg, sizeof(msg), "cudaPointerGetAttributes: %s", cudaGetErrorString(e));
-        return fc::set_error(FC_ERR_CUDA, msg);
-    }
-    if (at.type != cudaMemoryTypeDevice && at.type != cudaMemoryTypeManaged)
-        return fc::set_error(FC_ERR_INVALID_ARG, "a is not device memory");
-    e = cudaSetDevice(at.device);
-    if (e != cudaSuccess) {
-        snprintf(msg, sizeof(msg), "cudaSetDevice: %s", cudaGetErrorString(e));
-        return fc::set_error(FC_ERR_CUDA, msg);
-    }
+    // the device that owns the output is the one whose copy of the array is
+    // used; the caller's device is current again when this call returns
+    fc::DeviceScope scope;
+    st = scope.bind(a);
+    if (st != FC_OK) return st;
     void *ws = nullptr;
-    st = noalloc_workspace(at.device, &ws);
+    st = noalloc_workspace(scope.device(), &ws);
     if (st != FC_OK) return st;
     // The array keeps whatever the previous call left; the one part that must
-    // start at zero (the selection's count of finished blocks) is cleared on
-    // the stream, ahead of this step's kernels.
-    e = cudaMemsetAsync((char *)ws + fc::step_ws_counter_offset(N, chunk), 0, 256,
-                        (cudaStream_t)stream);
+    // start at zero (the selection's count of finished blocks and the staged
+    // reduction's failure word) is cleared on the stream, ahead of this
+    // step's kernels.
+    cudaError_t e = cudaMemsetAsync((char *)ws + fc::step_ws_counter_offset(N, chunk), 0, 256,
+                                    (cudaStream_t)stream);
     if (e != cudaSuccess) {
         snprintf(msg, sizeof(msg), "cudaMemsetAsync: %s", cudaGetErrorString(e));
         return fc::set_error(FC_ERR_CUDA, msg);

@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(SEL_THREADS)
              unsigned *__restrict__ done, float *norms, const int64_t k,
              int32_t *__restrict__ idx, uint8_t *__restrict__ mask,
              int32_t *__restrict__ slot, float *__restrict__ threshold,
-             unsigned *__restrict__ err)
+             unsigned *__restrict__ err, unsigned *__restrict__ status)
 {
     __shared__ uint32_t skeys[SEL_SMEM_KEYS];
     __shared__ uint32_t hist[256];
@@ -192,8 +192,11 @@ __global__ void __launch_bounds__(SEL_THREADS)
         __syncthreads();
         if (!s_last) return;
         // A wait inside the staged reduction gave up (not expected to
-        // happen): report it as a NaN threshold with nothing kept.
-        if (err && __ldcg(err) != 0u) {
+        // happen): report it as a NaN threshold with nothing kept, and mark
+        // the step as not applied, so that the update leaves the state alone.
+        const bool failed = err && __ldcg(err) != 0u;
+        if (tid == 0 && status) *status = failed ? 1u : 0u;
+        if (failed) {
             for (int64_t c = tid; c < C; c += SEL_THREADS) {
                 mask[c] = 0;
                 if (slot) slot[c] = -1;
@@ -305,7 +308,8 @@ __global__ void __launch_bounds__(SEL_THREADS)
 cudaError_t launch_select(const UnitGeom &G, const float *partials,
                           unsigned *done, float *norms, int64_t k,
                           int32_t *idx, uint8_t *mask, int32_t *slot,
-                          float *threshold, cudaStream_t s, unsigned *err)
+                          float *threshold, cudaStream_t s, unsigned *err,
+                          unsigned *status)
 {
     int64_t blocks = 1;
     if (partials) {
@@ -315,7 +319,7 @@ cudaError_t launch_select(const UnitGeom &G, const float *partials,
     }
     return launch_after_prior(k_select, (unsigned)blocks, SEL_THREADS, 0, s, G,
                               partials, done, norms, k, idx, mask, slot, threshold,
-                              err);
+                              err, status);
 }
 
 // ---- packed copy of the kept chunks ----------------------------------------------

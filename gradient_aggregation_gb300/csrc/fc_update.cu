@@ -43,12 +43,15 @@ __global__ void __launch_bounds__(FC_UPDATE_BLOCK)
              float *__restrict__ packed, __half *__restrict__ packed16,
              const float send_scale, const float lr, const float mu,
              float *r, float *__restrict__ v, float *__restrict__ w,
-             __half *__restrict__ w16, const int inplace)
+             __half *__restrict__ w16, const int inplace,
+             const unsigned *__restrict__ status)
 {
     const int64_t cs = G.cs;
     const bool pvec = (cs & 3) == 0;
     wait_for_prior_grid();
     allow_dependent_launch();  // the next step's reduction waits for us
+    // the selection marked the step as not applied: change nothing
+    if (status && __ldcg(status) != 0u) return;
     for (int64_t t = blockIdx.x; t < tiles; t += gridDim.x) {
         int64_t lo, hi, c, hin;
         const bool any = tile_range(G, t, lo, hi, c, hin);
@@ -146,12 +149,13 @@ cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           const uint8_t *mask, const int32_t *slot,
                           float *packed, __half *packed16, float send_scale,
                           float lr, float mu, float *r, float *v, float *w,
-                          __half *w16, bool inplace, cudaStream_t s)
+                          __half *w16, bool inplace, cudaStream_t s,
+                          const unsigned *status)
 {
     const int grid = grid_for((const void *)k_update, FC_UPDATE_BLOCK, 0, tiles);
     return launch_after_prior(k_update, (unsigned)grid, FC_UPDATE_BLOCK, 0, s, G, tiles,
                               a, mask, slot, packed, packed16, send_scale, lr,
-                              mu, r, v, w, w16, inplace ? 1 : 0);
+                              mu, r, v, w, w16, inplace ? 1 : 0, status);
 }
 
 }  // namespace fc

@@ -24,7 +24,8 @@ FC_ERR_INVALID_ARG = -1
 FC_ERR_ALIGNMENT = -2
 FC_ERR_WORKSPACE = -3
 FC_ERR_CUDA = -4
-FC_ERR_LIMIT = -5
+FC_ERR_TIMEOUT = -5
+FC_ERR_LIMIT = -6
 FC_MAX_TABLE_PTRS = 3072
 FC_MAX_TABLE_LAYERS = 512
 FC_NOALLOC_WORKSPACE_BYTES = 4 << 20
@@ -56,6 +57,8 @@ _SIGS = {
                                        _P, _P]),
     "fc_residual_sgd_update": (ctypes.c_int, [_P, _P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P]),
     "fc_step_workspace_size": (_SZ, [_I64, _I64]),
+    "fc_chunk_select_workspace": (_SZ, [_I64]),
+    "fc_step_status": (ctypes.c_int, [_P, _SZ, _I64, _I64, _P]),
     "fc_test_stage_loss": (ctypes.c_int, [_I64, ctypes.c_uint64]),
     "fc_step_reduce": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _P, _SZ, _P]),
     "fc_step_select": (ctypes.c_int, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -187,6 +190,10 @@ def fc_layout(sizes: Sequence[int]) -> Tuple[List[int], int]:
 
 def fc_step_workspace_size(N: int, chunk: int) -> int:
     return int(lib().fc_step_workspace_size(int(N), int(chunk)))
+
+
+def fc_chunk_select_workspace(C: int) -> int:
+    return int(lib().fc_chunk_select_workspace(int(C)))
 
 
 def fc_test_stage_loss(tile: int, wait_limit_ns: int = 20_000_000) -> None:
@@ -345,6 +352,18 @@ def fc_step(grads, loss_scale: float, chunk: int, k: int, lr: float, momentum: f
                          _p(workspace), workspace.numel(), _s(stream)))
 
 
+def fc_step_status(workspace: torch.Tensor, N: int, chunk: int, stream=None) -> int:
+    """Outcome of the last pipeline step on this workspace: FC_OK if it was
+    applied, FC_ERR_TIMEOUT if it was not (a bounded wait ran out).
+    Synchronises the stream; raises FcError only for bad arguments or a
+    failed CUDA call."""
+    st = int(lib().fc_step_status(_p(workspace), workspace.numel(), int(N), int(chunk),
+                                  _s(stream)))
+    if st not in (FC_OK, FC_ERR_TIMEOUT):
+        _check(st)
+    return st
+
+
 def fc_step_noalloc(grads, loss_scale: float, chunk: int, k: int, lr: float,
                     momentum: float, residual: torch.Tensor, a: torch.Tensor,
                     velocity: torch.Tensor, weights: torch.Tensor,
@@ -445,6 +464,10 @@ class Engine:
         fc_step_update(self.a, self.N, self.chunk, self.lr, self.momentum, self.residual,
                        self.velocity, self.weights, self.weights_fp16, self.mask, self.packed,
                        self.workspace, self.packed_fp16, self.send_scale, s)
+
+    def status(self, stream=None) -> int:
+        """FC_OK if the last step was applied, FC_ERR_TIMEOUT if not."""
+        return fc_step_status(self.workspace, self.N, self.chunk, stream)
 
     def state_dict(self) -> dict:
         return {"residual": self.residual.clone(), "velocity": self.velocity.clone(),

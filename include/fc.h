@@ -17,9 +17,9 @@
  *               precision, GradientFlow abstract) and unscaled by
  *               1/(loss scale * W)
  *   a3 norms    L2 norm of every fixed-size chunk of the fused vector
- *   a4 select   keep the top-k chunks ("only transmitting important gradient
- *               chunks", GradientFlow abstract: coarse-grained sparse
- *               communication) and compact them
+ *   a4 select   keep the k highest-norm chunks and compact them (GradientFlow
+ *               abstract: coarse-grained sparse communication sends only the
+ *               chunks that matter)
  *   a5 update   carry unkept values in an fp32 residual; momentum SGD on the
  *               fp32 master weights (FireCaffe §3 batched SGD, §6 each worker
  *               applies the summed update)
@@ -43,14 +43,16 @@
  *    host pointers are marked "host".  The library allocates nothing at run
  *    time.  Its state between calls is the thread-local error message,
  *    launch sizes cached per kernel and device, and the scratch array built
- *    into the library for fc_step_noalloc.
+ *    into the library for fc_step_noalloc (with its address per device).
  *  - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
  *    are asynchronous and stream-ordered; a returned FC_OK means the
  *    arguments were valid and the kernels were launched, not that they
- *    finished.  No call synchronises or queries the stream, so sequences
- *    can be captured in a CUDA graph (after one call outside capture has
- *    cached the launch configuration).  Kernels run on the device that owns
- *    the call's main device buffer (the output for most calls).
+ *    finished.  No call except fc_step_status synchronises or queries the
+ *    stream, so sequences can be captured in a CUDA graph (after one call
+ *    outside capture has cached the launch configuration).  Kernels run on
+ *    the device that owns the call's main device buffer (the output for
+ *    most calls); the caller's current device is the same after the call as
+ *    before it.
  *  - fp32 arrays and fp16 outputs must be 16-byte aligned; fp16 gradient
  *    inputs must be 2-byte aligned.  Otherwise FC_ERR_ALIGNMENT.  Which
  *    phase-1 kernel a layout of gradients gets (and so its speed, never its
@@ -82,7 +84,9 @@ typedef enum fc_status {
     FC_ERR_ALIGNMENT = -2,   /* a pointer breaks the alignment rule above */
     FC_ERR_WORKSPACE = -3,   /* workspace missing or smaller than required */
     FC_ERR_CUDA = -4,        /* a CUDA runtime call or launch failed */
-    FC_ERR_LIMIT = -5        /* a table exceeds the per-launch capacity */
+    FC_ERR_TIMEOUT = -5,     /* a bounded wait on the device ran out: the
+                                step was not applied (fc_step_status) */
+    FC_ERR_LIMIT = -6        /* a table or size exceeds a fixed capacity */
 } fc_status;
 
 /* Largest W*L and L that fc_fuse_pack / fc_step_reduce / fc_step accept in
@@ -181,6 +185,12 @@ FC_API fc_status fc_chunk_norms(const float *a, int64_t N, int64_t chunk,
                                 float *norms, void *stream);
 
 /* ---- a4: top-k selection and compaction -------------------------------------- */
+
+/* Bytes of caller workspace fc_chunk_select needs for C chunks: always 0.
+ * The selection keeps its histogram and scan state in shared memory of one
+ * block (the norms too, up to 11264 chunks; more are re-read from `norms`),
+ * so the call takes no workspace argument.  Returns 0 for any C. */
+FC_API size_t fc_chunk_select_workspace(int64_t C);
 
 /* Keeps the k chunks that come first in (norm descending, index ascending)
  * order, found by a radix select on the norms' bit patterns.
@@ -334,6 +344,25 @@ FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk,
                                 float send_scale, void *workspace,
                                 size_t workspace_bytes, void *stream);
 
+/* Outcome of the last pipeline step (fc_step, or fc_step_select and
+ * fc_step_update after phase 1) that used this workspace, read after
+ * `stream` has finished: the call copies one word back and synchronises
+ * the stream, so it is not for use while the stream is being captured.
+ *  FC_OK           the step was applied;
+ *  FC_ERR_TIMEOUT  a bounded wait inside the staged phase 1 ran out (not
+ *                  expected in normal operation: each wait allows 2 s).
+ *                  The step was then not applied: phase 2 reported a NaN
+ *                  threshold, an empty mask and idx = -1, and phase 3 left
+ *                  velocity, weights, the fp16 weights and the send buffers
+ *                  as they were.  With a separate `a` buffer the residual is
+ *                  unchanged too, so the step can simply be run again; in
+ *                  place (a == residual) phase 1 had already overwritten the
+ *                  residual with a for the tiles it reduced, so restore the
+ *                  residual before running the step again.
+ * Other statuses: bad arguments or a failed CUDA call. */
+FC_API fc_status fc_step_status(const void *workspace, size_t workspace_bytes,
+                                int64_t N, int64_t chunk, void *stream);
+
 /* Phases 1-3 in one call on one stream (three kernel launches). */
 FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                          const int64_t *sizes, float loss_scale, int64_t chunk,
@@ -364,12 +393,20 @@ FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
  * multiples of 256).  The call allocates nothing: no cudaMalloc, no
  * cudaFree, no allocating library routine.
  *
- * The first call on each device looks up the array's device address
- * (cudaGetSymbolAddress) with that device current and caches it; make that
- * first call before capturing a stream.  Every call shares the one array per
- * device: it clears the part that must start at zero on `stream` before its
+ * Every argument is checked before anything is queued on `stream`, so an
+ * invalid call queues nothing.
+ *
+ * The array's device address is looked up (cudaGetSymbolAddress) with the
+ * output's device current, and cached together with the identity of that
+ * device's current CUDA context.  The first call on a device, and the first
+ * call after cudaDeviceReset (which destroys the context and so moves the
+ * array), do the lookup: make those calls before capturing a stream.  Every
+ * call shares the one array per device and finds it as the last call left
+ * it: it clears the part that must start at zero on `stream` before its
  * kernels, but two calls whose work overlaps on the GPU (different streams
- * without ordering between them) race on the array and give wrong results. */
+ * without ordering between them) race on the array and give wrong results.
+ * A failed step (FC_ERR_TIMEOUT in fc_step_status) shows here as a NaN
+ * threshold with idx = -1. */
 FC_API fc_status fc_step_noalloc(const void *const *grads, int32_t W,
                                  int32_t L, const int64_t *sizes,
                                  float loss_scale, int64_t chunk, int64_t k,

@@ -124,6 +124,63 @@ def test_argument_errors_return_before_any_device_work(fc_lib):
     assert b"k = 5" in L.fc_last_error()
 
 
+def test_status_codes_match_the_header(fc_lib):
+    """The binding's status constants are the header's enum values, with the
+    timeout status at -5 and the capacity limit at -6."""
+    from gradient_aggregation_gb300 import fc
+    text = open(HEADER).read()
+    enum = dict((m.group(1), int(m.group(2)))
+                for m in re.finditer(r"\b(FC_(?:OK|ERR_\w+))\s*=\s*(-?\d+)", text))
+    assert enum == {"FC_OK": 0, "FC_ERR_INVALID_ARG": -1, "FC_ERR_ALIGNMENT": -2,
+                    "FC_ERR_WORKSPACE": -3, "FC_ERR_CUDA": -4, "FC_ERR_TIMEOUT": -5,
+                    "FC_ERR_LIMIT": -6}
+    for name, value in enum.items():
+        assert getattr(fc, name) == value, name
+    assert fc.fc_version() == 200
+
+
+def test_select_needs_no_workspace(fc_lib):
+    from gradient_aggregation_gb300 import fc
+    for C in (1, 520, 4096, 11264, 11265, 1 << 30):
+        assert fc.fc_chunk_select_workspace(C) == 0
+
+
+def test_noalloc_and_status_check_every_argument_before_device_work(fc_lib):
+    """fc_step_noalloc validates every argument (the same checks as fc_step)
+    before it looks up its scratch array or queues the clearing of it, so an
+    invalid call returns a status here, with no GPU in the process."""
+    from gradient_aggregation_gb300 import fc
+    L = fc_lib
+    P = ctypes.c_void_p
+    fake = 0x10000
+    arr = (ctypes.c_void_p * 4)(*([fake] * 4))
+    g = ctypes.cast(arr, P)
+    sizes = (ctypes.c_int64 * 2)(8, 8)
+
+    def noalloc(k=1, loss_scale=1.0, residual=fake, idx=fake, packed=None, send_scale=1.0,
+                chunk=4, W=2):
+        return L.fc_step_noalloc(g, W, 2, ctypes.cast(sizes, P), loss_scale, chunk, k, 0.1,
+                                 0.9, residual, fake, fake, fake, None, fake, idx, fake, packed,
+                                 None, send_scale, fake, None)
+    assert noalloc(k=5) == fc.FC_ERR_INVALID_ARG and b"k = 5" in L.fc_last_error()
+    assert noalloc(loss_scale=0.0) == fc.FC_ERR_INVALID_ARG
+    assert noalloc(residual=fake + 4) == fc.FC_ERR_ALIGNMENT
+    assert noalloc(idx=None) == fc.FC_ERR_INVALID_ARG
+    assert noalloc(packed=fake + 8) == fc.FC_ERR_ALIGNMENT
+    assert noalloc(send_scale=float("nan")) == fc.FC_ERR_INVALID_ARG
+    assert noalloc(chunk=0) == fc.FC_ERR_INVALID_ARG
+    assert noalloc(W=0) == fc.FC_ERR_INVALID_ARG
+    # the same checks in fc_step, before its workspace is looked at
+    assert L.fc_step(g, 2, 2, ctypes.cast(sizes, P), 0.0, 4, 1, 0.1, 0.9, fake, fake, fake,
+                     fake, None, fake, fake, fake, None, None, 1.0, fake, None, 0,
+                     None) == fc.FC_ERR_INVALID_ARG
+    # fc_step_status checks its workspace before reading it
+    assert L.fc_step_status(None, 10 ** 6, 16, 4, None) == fc.FC_ERR_WORKSPACE
+    assert L.fc_step_status(fake, 1, 16, 4, None) == fc.FC_ERR_WORKSPACE
+    assert L.fc_step_status(fake + 16, 10 ** 6, 16, 4, None) == fc.FC_ERR_ALIGNMENT
+    assert L.fc_step_status(fake, 10 ** 6, 0, 4, None) == fc.FC_ERR_INVALID_ARG
+
+
 def test_python_binding_raises_with_message(fc_lib):
     from gradient_aggregation_gb300 import fc
     with pytest.raises(fc.FcError) as e:

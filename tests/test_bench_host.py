@@ -124,3 +124,31 @@ def test_cpu_baseline_takes_the_median_of_several_oracle_steps():
     ref = oracle.step(g, st, ws.loss_scale, ws.chunk, ws.keep_percent, 100, ws.lr, ws.momentum)
     assert np.array_equal(ref["idx"], out["idx"])
     assert np.array_equal(st.weights.view(np.uint32), first.weights.view(np.uint32))
+
+
+def test_phase1_is_timed_at_least_twenty_times_at_any_step_count():
+    for steps in (20, 21, 50, 159, 160, 161, 2000, 50000):
+        every = bench.phase1_every(steps)
+        assert 1 <= every <= 8
+        assert len(range(0, steps, every)) >= bench.MIN_PHASE1
+    assert bench.phase1_every(2000) == 8 and bench.phase1_every(20) == 1
+
+
+def test_algorithmic_bytes_per_kernel():
+    """Phase 1 reads the gradients and the residual and writes `a` and one
+    fp32 sum of squares per 256-element unit; the plain count is N(2W+32)."""
+    from gradient_aggregation_gb300 import workload
+    wl = workload.get("alexnet")
+    W, N = wl.W, wl.N
+    units = bench.units_of(N, wl.chunk)
+    # 1904 chunks of 128 units, the last of 20840 elements: 82 units
+    assert units == 1903 * 128 + 82
+    b = bench.step_algorithmic_bytes(wl, 20)
+    assert b["phase1"] == 2 * W * N + 8 * N + 4 * units == 2_496_108_424
+    assert b["phase3"] == 16 * N + 8 * 20 * 32768 + 4 * 20 * 32768
+    assert b["survey"] == N * (2 * W + 32)
+    assert b["step"] == b["phase1"] + b["phase2"] + b["phase3"]
+    # keep-all: every element's a read, residual zeroed, send slots for all chunks
+    nin = workload.get("nin")
+    C = -(-nin.N // nin.chunk)
+    assert bench.step_algorithmic_bytes(nin, C)["phase3"] == 16 * nin.N + 8 * nin.N + 4 * C * nin.chunk

@@ -5,17 +5,18 @@ allocation after start-up).  It keeps its scratch in a fixed array built
 into libfc instead of a caller workspace.
 
 Its results must match fc_step with a caller workspace on the same inputs,
-over two calls in a row (the second call finds the array as the first one
-left it).  This file is collected last so that a failure here does not stop
-the other GPU tests.
+and the oracle, over two calls in a row (the second call finds the array as
+the first one left it).  This file is collected last so that a failure here
+does not stop the other GPU tests.
 """
 
 import numpy as np
 import pytest
 import torch
 
+import oracle
 from gradient_aggregation_gb300 import fc, workload
-from tests.gpu_util import GpuRun, bits_equal, dev_grads, assert_close, RTOL_F32
+from tests.gpu_util import GpuRun, bits_equal, dev_grads, assert_close, oracle_step, RTOL_F32
 
 pytestmark = pytest.mark.gpu
 
@@ -46,8 +47,10 @@ def test_noalloc_matches_workspace_pipeline_on_two_calls(name):
                              keep_percent=30, config_id=171, steps=2)
     ref = GpuRun(wl, "pipeline")      # fc_step with a caller workspace
     new = GpuRun(wl, "pipeline")      # same buffers, stepped by fc_step_noalloc
+    st = oracle.State(workload.initial_weights(wl))
     for step in range(2):
-        g = dev_grads(workload.all_grads(wl, step))
+        g_np = workload.all_grads(wl, step)
+        g = dev_grads(g_np)
         ref.step(g)
         _noalloc_step(new, g)
         a, b = ref.snapshot(), new.snapshot()
@@ -56,6 +59,29 @@ def test_noalloc_matches_workspace_pipeline_on_two_calls(name):
         for key in ("a", "residual", "velocity", "weights", "norms", "idx", "mask",
                     "packed", "packed16", "w16", "threshold"):
             assert bits_equal(np.asarray(a[key]), np.asarray(b[key])), (step, key)
+        # and against the oracle, element by element
+        oracle_step(g_np, st, wl, b)
+
+
+def test_noalloc_keeps_the_callers_current_device():
+    """The call runs on the device that owns its output and leaves the
+    caller's current device as it found it.  With two or more GPUs visible
+    the output lives on another device than the current one."""
+    wl = workload.get("tiny")
+    dev = 1 if torch.cuda.device_count() > 1 else 0
+    torch.cuda.set_device(0)
+    run = GpuRun(wl, "pipeline", device="cuda:%d" % dev)
+    g = dev_grads(workload.all_grads(wl, 0), device="cuda:%d" % dev)
+    with torch.cuda.device(dev):
+        stream = torch.cuda.current_stream().cuda_stream
+    fc.fc_step_noalloc(g, wl.loss_scale, wl.chunk, run.k, wl.lr, wl.momentum, run.residual,
+                       run.a, run.velocity, run.weights, run.w16, run.norms, run.idx,
+                       run.mask, run.packed, run.threshold, stream, run.packed16,
+                       run.send_scale)
+    assert torch.cuda.current_device() == 0
+    st = oracle.State(workload.initial_weights(wl))
+    with torch.cuda.device(dev):
+        oracle_step(workload.all_grads(wl, 0), st, wl, run.snapshot())
 
 
 def test_noalloc_rejects_problems_larger_than_its_array():
