@@ -156,6 +156,30 @@ __device__ __forceinline__ uint4 funnel8(const uint4 &a, const uint4 &b, int d)
     return make_uint4(w0, w1, w2, w3);
 }
 
+// Tile placement.  CTA b takes the tiles b, b + grid, b + 2 grid, ... except
+// where a swap pair sends a tile to another CTA: the two tiles of a pair
+// trade places (same round, different CTAs).  The host plans the swaps so
+// that tiles whose groups straddle a layer boundary (their elements are read
+// from global memory, which makes the tile several times slower) go to CTAs
+// with fewer tiles, at most one such tile each, instead of wherever the
+// cyclic order puts them.  Which CTA reduces a tile does not change any
+// result: every unit is reduced whole by one warp in the same order.
+constexpr int kMaxSwaps = 48;
+
+struct TileSwaps {
+    int32_t n;
+    int32_t a[kMaxSwaps], b[kMaxSwaps];
+};
+
+__device__ __forceinline__ int64_t placed_tile(const TileSwaps &sw, int64_t t)
+{
+    for (int i = 0; i < sw.n; ++i) {
+        if (sw.a[i] == t) return sw.b[i];
+        if (sw.b[i] == t) return sw.a[i];
+    }
+    return t;
+}
+
 }  // namespace
 
 // drop_tile >= 0 (test hook only, see fc_test_stage_loss): the producer
@@ -165,7 +189,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
                  float *partials, unsigned *err, const int64_t drop_tile,
-                 const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end)
+                 const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end,
+                 const TileSwaps swaps)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
@@ -196,12 +221,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         // producer
         if (lane != 0) return;
         int it = 0;
-        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        for (int64_t tc = blockIdx.x; tc < ntiles; tc += gridDim.x, ++it) {
             const int s = it % S;
             if (it >= S && !mbar_wait(smem_u32(&bars[S + s]), ((it / S) - 1) & 1, limit_ns)) {
                 atomicOr(err, 1u);
                 break;
             }
+            const int64_t t = placed_tile(swaps, tc);
             if (t == drop_tile) continue;
             const int64_t f0 = f_begin + t * TT;
             const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
@@ -283,12 +309,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // consumers
     int it = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    for (int64_t tc = blockIdx.x; tc < ntiles; tc += gridDim.x, ++it) {
         const int s = it % S;
         if (!mbar_wait(smem_u32(&bars[s]), (it / S) & 1, limit_ns)) {
             if (lane == 0) atomicOr(err, 4u);
             return;
         }
+        const int64_t t = placed_tile(swaps, tc);
         const int64_t f0 = f_begin + t * TT;
         const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
         const unsigned char *st = stages + (size_t)s * sbytes;
@@ -440,6 +467,89 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
     return tiles >= FC_TMA_REGISTER_MIN_TILES ? 0 : 1;
 }
 
+// Plans the tile swaps (see TileSwaps) for the shifted layout: tiles of TT
+// elements over [fb, fe), `grid` CTAs.  A tile's weight is the number of
+// layer boundaries inside it that do not fall on a multiple of 8 fused
+// elements (each puts one or two groups of 8 on the global-memory path);
+// such a tile counts as 1 + weight tiles of work.  Greedy, heaviest tile
+// first: each goes to the CTA with the least work so far (its own CTA if
+// that is one of them), trading places with a plain tile of that CTA in the
+// nearest round.
+template <class Tab>
+static void plan_swaps(const Tab &tab, int64_t fb, int64_t fe, int TT, int grid,
+                       TileSwaps &sw)
+{
+    sw.n = 0;
+    const int64_t T = (fe - fb + TT - 1) / TT;
+    if (grid < 2 || T <= grid || T >= ((int64_t)1 << 31)) return;
+    // heavy tiles and their weights (ascending tile order)
+    int64_t heavy_t[FC_MAX_TABLE_LAYERS];
+    int heavy_w[FC_MAX_TABLE_LAYERS];
+    int nh = 0;
+    for (int l = 1; l < tab.L; ++l) {
+        const int64_t o = tab.off[l];
+        if (o <= fb || o >= fe || (o & 7) == 0) continue;
+        const int64_t t = (o - fb) / TT;
+        if (nh > 0 && heavy_t[nh - 1] == t) {
+            ++heavy_w[nh - 1];
+        } else if (nh < FC_MAX_TABLE_LAYERS) {
+            heavy_t[nh] = t;
+            heavy_w[nh] = 1;
+            ++nh;
+        }
+    }
+    if (nh == 0) return;
+    // heaviest first (insertion sort, at most a few hundred entries)
+    for (int i = 1; i < nh; ++i)
+        for (int j = i; j > 0 && heavy_w[j] > heavy_w[j - 1]; --j) {
+            const int64_t tt = heavy_t[j]; heavy_t[j] = heavy_t[j - 1]; heavy_t[j - 1] = tt;
+            const int ww = heavy_w[j]; heavy_w[j] = heavy_w[j - 1]; heavy_w[j - 1] = ww;
+        }
+    // work per CTA with every heavy tile still unplaced (counted as plain)
+    static thread_local int64_t cost[1024];
+    if (grid > 1024) return;
+    const int64_t full = T / grid, extra = T % grid;
+    for (int b = 0; b < grid; ++b) cost[b] = full + (b < extra ? 1 : 0);
+    auto is_heavy = [&](int64_t t) {
+        for (int i = 0; i < nh; ++i)
+            if (heavy_t[i] == t) return true;
+        return false;
+    };
+    auto is_swapped = [&](int64_t t) {
+        for (int i = 0; i < sw.n; ++i)
+            if (sw.a[i] == t || sw.b[i] == t) return true;
+        return false;
+    };
+    for (int i = 0; i < nh; ++i) {
+        const int64_t t = heavy_t[i];
+        const int owner = (int)(t % grid);
+        int best = owner;
+        for (int b = 0; b < grid; ++b)
+            if (cost[b] < cost[best]) best = b;
+        if (best != owner && sw.n < kMaxSwaps) {
+            // a plain tile of CTA `best` in the round of t, or the nearest round
+            const int64_t r0 = t / grid;
+            int64_t partner = -1;
+            for (int64_t d = 0; d <= full + 1 && partner < 0; ++d) {
+                for (int sgn = 0; sgn < 2 && partner < 0; ++sgn) {
+                    const int64_t r = sgn ? r0 + d : r0 - d;
+                    if (r < 0 || (sgn && d == 0)) continue;
+                    const int64_t p = r * grid + best;
+                    if (p < T && !is_heavy(p) && !is_swapped(p)) partner = p;
+                }
+            }
+            if (partner >= 0) {
+                sw.a[sw.n] = (int32_t)t;
+                sw.b[sw.n] = (int32_t)partner;
+                ++sw.n;
+            } else {
+                best = owner;
+            }
+        }
+        cost[best] += heavy_w[i];
+    }
+}
+
 template <class Tab, int WT, int MAXH, bool MIS>
 static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                                 const float *resid, float *out, float *partials,
@@ -465,10 +575,15 @@ static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
     }
     const int64_t tiles = (fe - fb + TT - 1) / TT;
     const int grid = grid_for((const void *)kern, kThreads, smem, tiles);
+    TileSwaps swaps;
+    if (MIS)
+        plan_swaps(tab, fb, fe, TT, grid, swaps);
+    else
+        swaps.n = 0;
     const int64_t drop = g_drop_tile.exchange(-1);
     const uint64_t limit = drop >= 0 ? g_drop_limit_ns.load() : kWaitLimitNs;
     return launch_after_prior(kern, (unsigned)grid, kThreads, smem, s, tab, G, TT, S, u,
-                              resid, out, partials, err, drop, limit, fb, fe);
+                              resid, out, partials, err, drop, limit, fb, fe, swaps);
 }
 
 template <class Tab, bool MIS>
