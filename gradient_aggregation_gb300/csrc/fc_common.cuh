@@ -156,6 +156,21 @@ __device__ __forceinline__ void unpack8(const uint4 &q, float (&x)[8])
     }
 }
 
+// 8 fp16 values starting `d` halves (0..7) into the 16 halves a:b.
+__device__ __forceinline__ uint4 funnel8(const uint4 &a, const uint4 &b, int d)
+{
+    uint32_t w0 = a.x, w1 = a.y, w2 = a.z, w3 = a.w, w4 = b.x, w5 = b.y, w6 = b.z, w7 = b.w;
+    if (d & 4) { w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7; }
+    if (d & 2) { w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5; }
+    if (d & 1) {
+        w0 = __funnelshift_r(w0, w1, 16);
+        w1 = __funnelshift_r(w1, w2, 16);
+        w2 = __funnelshift_r(w2, w3, 16);
+        w3 = __funnelshift_r(w3, w4, 16);
+    }
+    return make_uint4(w0, w1, w2, w3);
+}
+
 // ---- the binary reduction tree over the workers ------------------------------
 //
 // Level-order adjacent pairing with an odd element carried up equals the

@@ -5,11 +5,15 @@
 // buffer is worker w's layers concatenated in order (no padding).
 //
 // GB300 mapping: one grid row (blockIdx.y) per worker; each thread writes one
-// 16-byte-aligned group of 8 destination elements with a single 16-byte store
-// and reads its source with one 16-byte streaming load when the source is
-// aligned the same way, else element by element.  Groups at the ends of a row
-// (when N is not a multiple of 8) are stored element by element so that two
-// rows never write the same 16 bytes.
+// 16-byte-aligned group of 8 destination elements with a single 16-byte store.
+// A group whose 8 source elements lie in one layer is read with one 16-byte
+// streaming load when the source is 16-byte aligned, else with the two
+// aligned 16-byte words that hold it and a funnel shift (both words hold at
+// least one byte of the layer, so neither leaves the layer's pages; the
+// neighbouring thread reads the same words, so the second one mostly hits in
+// L1).  Only groups that straddle a layer boundary are read element by
+// element.  Groups at the ends of a row (when N is not a multiple of 8) are
+// stored element by element so that two rows never write the same 16 bytes.
 #include "fc_internal.h"
 
 namespace fc {
@@ -34,6 +38,10 @@ __global__ void __launch_bounds__(FC_BLOCK)
             uint4 val;
             if (f0 + 8 <= tab.off[l + 1] && (((uintptr_t)src & 15u) == 0)) {
                 val = ld_stream16(src, pol);
+            } else if (f0 + 8 <= tab.off[l + 1]) {
+                const uintptr_t at = (uintptr_t)src;
+                const uint4 *q = reinterpret_cast<const uint4 *>(at & ~(uintptr_t)15);
+                val = funnel8(__ldg(q), __ldg(q + 1), (int)((at & 15u) >> 1));
             } else {
                 unsigned short h[8];
 #pragma unroll

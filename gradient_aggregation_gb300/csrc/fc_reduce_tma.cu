@@ -141,45 +141,6 @@ __device__ __forceinline__ int layer_shift(const Tab &tab, int l)
     return (int)((((uintptr_t)tab.ptr[l]) - 2u * (uintptr_t)tab.off[l]) >> 1) & 7;
 }
 
-// 8 fp16 values starting `d` halves (0..7) into the 16 halves a:b.
-__device__ __forceinline__ uint4 funnel8(const uint4 &a, const uint4 &b, int d)
-{
-    uint32_t w0 = a.x, w1 = a.y, w2 = a.z, w3 = a.w, w4 = b.x, w5 = b.y, w6 = b.z, w7 = b.w;
-    if (d & 4) { w0 = w2; w1 = w3; w2 = w4; w3 = w5; w4 = w6; w5 = w7; }
-    if (d & 2) { w0 = w1; w1 = w2; w2 = w3; w3 = w4; w4 = w5; }
-    if (d & 1) {
-        w0 = __funnelshift_r(w0, w1, 16);
-        w1 = __funnelshift_r(w1, w2, 16);
-        w2 = __funnelshift_r(w2, w3, 16);
-        w3 = __funnelshift_r(w3, w4, 16);
-    }
-    return make_uint4(w0, w1, w2, w3);
-}
-
-// Tile placement.  CTA b takes the tiles b, b + grid, b + 2 grid, ... except
-// where a swap pair sends a tile to another CTA: the two tiles of a pair
-// trade places (same round, different CTAs).  The host plans the swaps so
-// that tiles whose groups straddle a layer boundary (their elements are read
-// from global memory, which makes the tile several times slower) go to CTAs
-// with fewer tiles, at most one such tile each, instead of wherever the
-// cyclic order puts them.  Which CTA reduces a tile does not change any
-// result: every unit is reduced whole by one warp in the same order.
-constexpr int kMaxSwaps = 48;
-
-struct TileSwaps {
-    int32_t n;
-    int32_t a[kMaxSwaps], b[kMaxSwaps];
-};
-
-__device__ __forceinline__ int64_t placed_tile(const TileSwaps &sw, int64_t t)
-{
-    for (int i = 0; i < sw.n; ++i) {
-        if (sw.a[i] == t) return sw.b[i];
-        if (sw.b[i] == t) return sw.a[i];
-    }
-    return t;
-}
-
 }  // namespace
 
 // drop_tile >= 0 (test hook only, see fc_test_stage_loss): the producer
@@ -189,8 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
                  float *partials, unsigned *err, const int64_t drop_tile,
-                 const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end,
-                 const TileSwaps swaps)
+                 const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
@@ -221,13 +181,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         // producer
         if (lane != 0) return;
         int it = 0;
-        for (int64_t tc = blockIdx.x; tc < ntiles; tc += gridDim.x, ++it) {
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
             const int s = it % S;
             if (it >= S && !mbar_wait(smem_u32(&bars[S + s]), ((it / S) - 1) & 1, limit_ns)) {
                 atomicOr(err, 1u);
                 break;
             }
-            const int64_t t = placed_tile(swaps, tc);
             if (t == drop_tile) continue;
             const int64_t f0 = f_begin + t * TT;
             const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
@@ -251,7 +210,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // if unstaged), layer, copied range [lo, hi) of the row as
                 // lo | hi << 16}.  The last entry always ends at the tile's end.
                 int4 *pieces = reinterpret_cast<int4 *>(st + gbytes + (size_t)TT * 4);
-                int n = 0, gap = 0, prev_d = -1;
+                int n = 0;
+                int64_t prev_phi = 0;  // end of the last staged piece's frames
                 uint32_t row_bytes = 0;
                 int l = find_layer(tab, f0);
                 for (int64_t fa = f0; fa < f1;) {
@@ -261,26 +221,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                         pieces[n++] = make_int4((int)(f1 - f0), -1, l, 0);
                         break;
                     }
+                    // The piece is copied as the whole 16-byte frames that
+                    // hold it, including the partial frames at a layer's ends
+                    // (every frame holds at least one element of the layer,
+                    // so no copy reaches a page the layer does not touch).
+                    // Its gap is the smallest multiple of 8 that puts its
+                    // first frame after the last frame of the piece before.
                     const int d = layer_shift(tab, l);
-                    const int g = gap + (prev_d > d ? 8 : 0);
+                    const int64_t x = fa - f0;
+                    int64_t g = prev_phi - round_down8(x + d);
+                    g = g > 0 ? round_up8(g) : 0;
                     const int64_t sh = g + d;
-                    // copied row range: the 16-byte frames around the piece,
-                    // clipped to the layer's own elements
-                    int64_t plo = round_down8(fa - f0 + sh);
-                    const int64_t lay_lo = tab.off[l] - f0 + sh;
-                    if (plo < lay_lo) plo = round_up8(lay_lo);
-                    int64_t phi = round_up8(fb - f0 + sh);
-                    const int64_t lay_hi = tab.off[l + 1] - f0 + sh;
-                    if (phi > lay_hi) phi = round_down8(lay_hi);
+                    const int64_t plo = round_down8(x + sh);
+                    const int64_t phi = round_up8(fb - f0 + sh);
                     if (phi > ROW) {
                         pieces[n++] = make_int4((int)(fb - f0), -1, l, 0);
                     } else {
-                        if (phi < plo) phi = plo;
                         pieces[n++] = make_int4((int)(fb - f0), (int)sh, l,
                                                 (int)(plo | (phi << 16)));
                         row_bytes += (uint32_t)(phi - plo) * 2;
-                        gap = g;
-                        prev_d = d;
+                        prev_phi = phi;
                     }
                     fa = fb;
                 }
@@ -309,13 +269,12 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     // consumers
     int it = 0;
-    for (int64_t tc = blockIdx.x; tc < ntiles; tc += gridDim.x, ++it) {
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
         const int s = it % S;
         if (!mbar_wait(smem_u32(&bars[s]), (it / S) & 1, limit_ns)) {
             if (lane == 0) atomicOr(err, 4u);
             return;
         }
-        const int64_t t = placed_tile(swaps, tc);
         const int64_t f0 = f_begin + t * TT;
         const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
         const unsigned char *st = stages + (size_t)s * sbytes;
@@ -337,10 +296,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                 } else {
                     const int uu = (int)off;
                     const int4 *pieces = reinterpret_cast<const int4 *>(st + gbytes + (size_t)TT * 4);
+                    int i = 0;
                     int4 pc = pieces[0];
-                    for (int i = 1; pc.x <= uu; ++i) pc = pieces[i];
-                    const int plo = pc.w & 0xffff, phi = pc.w >> 16;
-                    if (pc.y >= 0 && uu + 8 <= pc.x && uu + pc.y >= plo && uu + pc.y + 8 <= phi) {
+                    while (pc.x <= uu) pc = pieces[++i];
+                    const int alo = pc.w & 0xffff, ahi = pc.w >> 16;
+                    // a group that runs past its piece (a layer boundary) takes
+                    // the next piece too; the last piece ends at the tile's end
+                    const int split = uu + 8 <= pc.x ? 8 : pc.x - uu;
+                    const int4 pn = pieces[split < 8 ? i + 1 : i];
+                    const int blo = pn.w & 0xffff, bhi = pn.w >> 16;
+                    if (split == 8 && pc.y >= 0 && uu + pc.y >= alo && uu + pc.y + 8 <= ahi) {
                         // all 8 in one copied piece: two aligned loads, shifted
                         const int p0 = uu + (pc.y & ~7), d = pc.y & 7;
                         tree_sum<WT, MAXH, 8>(
@@ -352,28 +317,40 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 unpack8(d ? funnel8(qa, q[1], d) : qa, x);
                             },
                             a);
-                    } else {
-                        // at a layer boundary (or unstaged): from global memory.
-                        // Within two layers: two pointers per worker, all 8
-                        // elements of a worker loaded together.
-                        int la = pc.z;
-                        while (tab.off[la + 1] <= f) ++la;
-                        int lb = la;
-                        while (tab.off[lb + 1] <= f + 7) ++lb;
-                        if (lb - la <= 1) {
-                            const int64_t ja = f - tab.off[la], jb = f - tab.off[lb];
-                            const int split = (int)(tab.off[la + 1] - f < 8 ? tab.off[la + 1] - f : 8);
-                            tree_sum<WT, MAXH, 8>(
-                                W,
-                                [&](int w, float(&x)[8]) {
-                                    const __half *pa = tab.ptr[w * L + la] + ja;
-                                    const __half *pb = tab.ptr[w * L + lb] + jb;
+                    } else if (split < 8 && pc.y >= 0 && pn.y >= 0 && uu + pc.y >= alo &&
+                               uu + pc.y + split <= ahi && uu + split + pn.y >= blo &&
+                               uu + 8 + pn.y <= bhi && uu + 8 <= pn.x) {
+                        // at a layer boundary, both pieces staged: elements
+                        // e < split from piece pc, the rest from piece pn, each
+                        // read as two aligned 16-byte words and a funnel shift
+                        const int pa = uu + (pc.y & ~7), da = pc.y & 7;
+                        const int pb = uu + (pn.y & ~7), db = pn.y & 7;
+                        // word j holds elements 2j, 2j+1: mask of the halves from pc
+                        uint32_t m[4];
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e)
-                                        x[e] = ld_half_as_float(e < split ? pa + e : pb + e);
-                                },
-                                a);
-                        } else {
+                        for (int j = 0; j < 4; ++j)
+                            m[j] = 2 * j + 1 < split ? 0xffffffffu : (2 * j < split ? 0x0000ffffu : 0u);
+                        tree_sum<WT, MAXH, 8>(
+                            W,
+                            [&](int w, float(&x)[8]) {
+                                const unsigned char *row = st + (size_t)w * ROW * 2;
+                                const uint4 *qa = reinterpret_cast<const uint4 *>(row + (size_t)pa * 2);
+                                const uint4 *qb = reinterpret_cast<const uint4 *>(row + (size_t)pb * 2);
+                                uint4 v = qa[0], vb = qb[0];
+                                if (da) v = funnel8(v, qa[1], da);
+                                if (db) vb = funnel8(vb, qb[1], db);
+                                v.x = (v.x & m[0]) | (vb.x & ~m[0]);
+                                v.y = (v.y & m[1]) | (vb.y & ~m[1]);
+                                v.z = (v.z & m[2]) | (vb.z & ~m[2]);
+                                v.w = (v.w & m[3]) | (vb.w & ~m[3]);
+                                unpack8(v, x);
+                            },
+                            a);
+                    } else {
+                        // unstaged pieces (a tile with more pieces than the
+                        // table holds, or past the row's slack) or a group over
+                        // three or more layers: element by element from
+                        // global memory
                         int l = pc.z;
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
@@ -387,7 +364,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                                 },
                                 s1);
                             a[e] = s1[0];
-                        }
                         }
                     }
                 }
@@ -467,89 +443,6 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
     return tiles >= FC_TMA_REGISTER_MIN_TILES ? 0 : 1;
 }
 
-// Plans the tile swaps (see TileSwaps) for the shifted layout: tiles of TT
-// elements over [fb, fe), `grid` CTAs.  A tile's weight is the number of
-// layer boundaries inside it that do not fall on a multiple of 8 fused
-// elements (each puts one or two groups of 8 on the global-memory path);
-// such a tile counts as 1 + weight tiles of work.  Greedy, heaviest tile
-// first: each goes to the CTA with the least work so far (its own CTA if
-// that is one of them), trading places with a plain tile of that CTA in the
-// nearest round.
-template <class Tab>
-static void plan_swaps(const Tab &tab, int64_t fb, int64_t fe, int TT, int grid,
-                       TileSwaps &sw)
-{
-    sw.n = 0;
-    const int64_t T = (fe - fb + TT - 1) / TT;
-    if (grid < 2 || T <= grid || T >= ((int64_t)1 << 31)) return;
-    // heavy tiles and their weights (ascending tile order)
-    int64_t heavy_t[FC_MAX_TABLE_LAYERS];
-    int heavy_w[FC_MAX_TABLE_LAYERS];
-    int nh = 0;
-    for (int l = 1; l < tab.L; ++l) {
-        const int64_t o = tab.off[l];
-        if (o <= fb || o >= fe || (o & 7) == 0) continue;
-        const int64_t t = (o - fb) / TT;
-        if (nh > 0 && heavy_t[nh - 1] == t) {
-            ++heavy_w[nh - 1];
-        } else if (nh < FC_MAX_TABLE_LAYERS) {
-            heavy_t[nh] = t;
-            heavy_w[nh] = 1;
-            ++nh;
-        }
-    }
-    if (nh == 0) return;
-    // heaviest first (insertion sort, at most a few hundred entries)
-    for (int i = 1; i < nh; ++i)
-        for (int j = i; j > 0 && heavy_w[j] > heavy_w[j - 1]; --j) {
-            const int64_t tt = heavy_t[j]; heavy_t[j] = heavy_t[j - 1]; heavy_t[j - 1] = tt;
-            const int ww = heavy_w[j]; heavy_w[j] = heavy_w[j - 1]; heavy_w[j - 1] = ww;
-        }
-    // work per CTA with every heavy tile still unplaced (counted as plain)
-    static thread_local int64_t cost[1024];
-    if (grid > 1024) return;
-    const int64_t full = T / grid, extra = T % grid;
-    for (int b = 0; b < grid; ++b) cost[b] = full + (b < extra ? 1 : 0);
-    auto is_heavy = [&](int64_t t) {
-        for (int i = 0; i < nh; ++i)
-            if (heavy_t[i] == t) return true;
-        return false;
-    };
-    auto is_swapped = [&](int64_t t) {
-        for (int i = 0; i < sw.n; ++i)
-            if (sw.a[i] == t || sw.b[i] == t) return true;
-        return false;
-    };
-    for (int i = 0; i < nh; ++i) {
-        const int64_t t = heavy_t[i];
-        const int owner = (int)(t % grid);
-        int best = owner;
-        for (int b = 0; b < grid; ++b)
-            if (cost[b] < cost[best]) best = b;
-        if (best != owner && sw.n < kMaxSwaps) {
-            // a plain tile of CTA `best` in the round of t, or the nearest round
-            const int64_t r0 = t / grid;
-            int64_t partner = -1;
-            for (int64_t d = 0; d <= full + 1 && partner < 0; ++d) {
-                for (int sgn = 0; sgn < 2 && partner < 0; ++sgn) {
-                    const int64_t r = sgn ? r0 + d : r0 - d;
-                    if (r < 0 || (sgn && d == 0)) continue;
-                    const int64_t p = r * grid + best;
-                    if (p < T && !is_heavy(p) && !is_swapped(p)) partner = p;
-                }
-            }
-            if (partner >= 0) {
-                sw.a[sw.n] = (int32_t)t;
-                sw.b[sw.n] = (int32_t)partner;
-                ++sw.n;
-            } else {
-                best = owner;
-            }
-        }
-        cost[best] += heavy_w[i];
-    }
-}
-
 template <class Tab, int WT, int MAXH, bool MIS>
 static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                                 const float *resid, float *out, float *partials,
@@ -575,15 +468,10 @@ static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
     }
     const int64_t tiles = (fe - fb + TT - 1) / TT;
     const int grid = grid_for((const void *)kern, kThreads, smem, tiles);
-    TileSwaps swaps;
-    if (MIS)
-        plan_swaps(tab, fb, fe, TT, grid, swaps);
-    else
-        swaps.n = 0;
     const int64_t drop = g_drop_tile.exchange(-1);
     const uint64_t limit = drop >= 0 ? g_drop_limit_ns.load() : kWaitLimitNs;
     return launch_after_prior(kern, (unsigned)grid, kThreads, smem, s, tab, G, TT, S, u,
-                              resid, out, partials, err, drop, limit, fb, fe, swaps);
+                              resid, out, partials, err, drop, limit, fb, fe);
 }
 
 template <class Tab, bool MIS>

@@ -175,9 +175,9 @@ __global__ void __launch_bounds__(SEL_THREADS)
              unsigned *__restrict__ err, unsigned *__restrict__ status)
 {
     __shared__ uint32_t skeys[SEL_SMEM_KEYS];
-    __shared__ uint32_t hist[256];
+    __shared__ uint32_t hist[3][256];
     __shared__ uint64_t sw[32];
-    __shared__ uint32_t s_digit, s_rem, s_last;
+    __shared__ uint32_t s_last, s_dr[2];
     const int tid = threadIdx.x;
     const int64_t C = G.C;
     wait_for_prior_grid();
@@ -190,11 +190,12 @@ __global__ void __launch_bounds__(SEL_THREADS)
             const float n = chunk_norm_from_units(G, partials, c, lane);
             if (lane == 0) norms[c] = n;
         }
-        // publish this block's norms before counting it: the writers fence,
-        // the barrier orders them before the count
-        if (lane == 0) __threadfence();
+        // publish this block's norms before counting it: the barrier orders
+        // every warp's writes before thread 0's fence, which makes them
+        // visible device-wide before the count
         __syncthreads();
         if (tid == 0) {
+            __threadfence();
             const unsigned seen = atomicAdd(done, 1u);
             s_last = seen == gridDim.x - 1 ? 1u : 0u;
             if (s_last) {
@@ -233,51 +234,82 @@ __global__ void __launch_bounds__(SEL_THREADS)
         return in_smem ? skeys[c] : __float_as_uint(__ldcg(norms + c));
     };
 
+    const int lane = tid & 31;
+    if (k == C) {
+        // Every chunk is kept: the threshold is the smallest norm, and chunk
+        // c goes to slot c.  (The radix select and the scan below would give
+        // the same outputs.)
+        uint32_t lo = 0xffffffffu;
+        for (int64_t c = tid; c < C; c += SEL_THREADS) {
+            lo = min(lo, key_at(c));
+            mask[c] = 1;
+            if (slot) slot[c] = (int32_t)c;
+            idx[c] = (int32_t)c;
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+        if (lane == 0) hist[0][tid >> 5] = lo;
+        __syncthreads();
+        if (tid < 32) {
+            lo = hist[0][tid];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) lo = min(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            if (tid == 0) threshold[0] = __uint_as_float(lo);
+        }
+        return;
+    }
+
+    // Radix passes.  Pass p counts into hist[p % 3] while the threads below
+    // 256 clear hist[(p + 1) % 3] for the next pass (last read by the scan of
+    // pass p - 2, finished before that pass's second barrier), so a pass
+    // needs two barriers: after the counts, and after warp 0 has found the
+    // digit.
+    if (tid < 256) hist[0][tid] = 0;
+    __syncthreads();
     uint32_t prefix = 0, rem = (uint32_t)k;
 #pragma unroll 1
     for (int pass = 0; pass < 4; ++pass) {
         const int shift = 24 - 8 * pass;
-        if (tid < 256) hist[tid] = 0;
-        __syncthreads();
+        uint32_t *h = hist[pass % 3];
+        if (tid < 256) hist[(pass + 1) % 3][tid] = 0;
         // Norms of similar size share their top bits, so many lanes hit the
         // same bin: lanes with equal digits are counted once per warp.
         for (int64_t base = tid & ~31; base < C; base += SEL_THREADS) {
-            const int64_t c = base + (tid & 31);
+            const int64_t c = base + lane;
             const uint32_t key = c < C ? key_at(c) : 0u;
             const bool in = c < C && (pass == 0 || (key >> (shift + 8)) == prefix);
             const uint32_t digit = in ? (key >> shift) & 255u : 256u;
             const uint32_t peers = __match_any_sync(0xffffffffu, digit);
-            if (in && (tid & 31) == __ffs(peers) - 1)
-                atomicAdd(&hist[digit], (uint32_t)__popc(peers));
+            if (in && lane == __ffs(peers) - 1)
+                atomicAdd(&h[digit], (uint32_t)__popc(peers));
         }
         __syncthreads();
         if (tid < 32) {
-            // lane t owns bins 255-8t .. 248-8t, from the top down
-            uint32_t h[8], local = 0;
+            uint32_t hv[8], local = 0;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                h[i] = hist[255 - 8 * tid - i];
-                local += h[i];
+                hv[i] = h[255 - 8 * lane - i];
+                local += hv[i];
             }
             uint32_t inc = local;
 #pragma unroll
             for (int o = 1; o < 32; o <<= 1) {
                 const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
-                if (tid >= o) inc += y;
+                if (lane >= o) inc += y;
             }
-            uint32_t above = inc - local;  // keys in higher bins
+            uint32_t above = inc - local;
 #pragma unroll
             for (int i = 0; i < 8; ++i) {
-                if (above < rem && rem <= above + h[i]) {
-                    s_digit = (uint32_t)(255 - 8 * tid - i);
-                    s_rem = rem - above;
+                if (above < rem && rem <= above + hv[i]) {
+                    s_dr[0] = (uint32_t)(255 - 8 * lane - i);
+                    s_dr[1] = rem - above;
                 }
-                above += h[i];
+                above += hv[i];
             }
         }
         __syncthreads();
-        prefix = (prefix << 8) | s_digit;
-        rem = s_rem;
+        prefix = (prefix << 8) | s_dr[0];
+        rem = s_dr[1];
     }
     const uint32_t tau = prefix;  // bit pattern of the k-th largest norm
     const uint32_t need = rem;    // chunks equal to tau that are kept
