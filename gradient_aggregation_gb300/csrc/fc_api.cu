@@ -74,9 +74,11 @@ UnitGeom ugeom(int64_t N, int64_t cs)
 size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 
 // Workspace of the pipeline: unit sums (float [units]), a 256-byte block of
-// words (0: the selection's count of finished blocks, zero between calls;
-// 1: the staged reduction's failure word, zero between calls; 2: the last
-// step's outcome, 0 = applied) and the kept-slot map (int32 [C]).
+// 32-bit words (0: the selection's count of finished blocks; 1: the staged
+// reduction's failure word; 2: the last step's outcome, 0 = applied; 4-5:
+// the staged reduction's 64-bit counter of dynamically handed-out tiles; 6:
+// its count of finished producers; all but word 2 zero between calls) and
+// the kept-slot map (int32 [C]).
 struct WsLayout {
     size_t partials, counters, slot, total;
 };
@@ -453,7 +455,7 @@ static fc_status reduce_span(const char *name, const void *const *grads, int32_t
     const UnitGeom G = ugeom(N, chunk);
     const WsLayout wl = ws_layout(N, chunk);
     float *partials = (float *)((char *)workspace + wl.partials);
-    unsigned *err = (unsigned *)((char *)workspace + wl.counters) + 1;
+    unsigned *ctr = (unsigned *)((char *)workspace + wl.counters);
     const int64_t ub = first_unit_at(G, f_begin), ue = first_unit_at(G, f_end);
     if (ub >= ue) return ok();
     cudaError_t e;
@@ -462,7 +464,7 @@ static fc_status reduce_span(const char *name, const void *const *grads, int32_t
             // chunk % 256 == 0 here: unit j starts at 256 j
             const int64_t fb = ub * FC_UNIT;
             const int64_t fe = ue * FC_UNIT < N ? ue * FC_UNIT : N;
-            return launch_reduce_tma(tab, G, u, residual, a, partials, err,
+            return launch_reduce_tma(tab, G, u, residual, a, partials, ctr,
                                      (cudaStream_t)stream, lay, fb, fe);
         }
         return launch_reduce(tab, G, u, residual, a, partials, (cudaStream_t)stream, order,

@@ -25,8 +25,9 @@ cudaError_t launch_reduce(const Tab &tab, const UnitGeom &G, float u,
 
 // TMA-staged phase 1 (tree order only).  tma_layout: 0 if the layout does
 // not allow it, 1 for the aligned layout, 2 for the shifted one (layers at
-// any offset, one address shift per layer for all workers).  err: a device
-// word set if a wait inside the kernel gave up.
+// any offset, one address shift per layer for all workers).  ctr: the
+// pipeline workspace's 256-byte block of counter words (zero on entry and
+// on exit but for word 1, which is set if a wait inside the kernel gave up).
 template <class Tab>
 int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials);
 // The staged kernel works on whole 256-element units: fused elements
@@ -35,7 +36,7 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials);
 template <class Tab>
 cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
                               const float *resid, float *out, float *partials,
-                              unsigned *err, cudaStream_t s, int layout, int64_t fb = 0,
+                              unsigned *ctr, cudaStream_t s, int layout, int64_t fb = 0,
                               int64_t fe = -1);
 
 template <class Tab>

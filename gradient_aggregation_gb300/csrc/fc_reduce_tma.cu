@@ -31,9 +31,21 @@
 //    it measured faster on long runs.  Aligned mid-size runs go to the
 //    register kernel instead (see tma_layout).
 //
+// Tile order: CTA b takes tiles b, b + grid, b + 2 grid, ...  In long
+// launches (kDynMinRounds rounds or more) that holds for all but the last
+// kDynRounds rounds; the tiles after those are handed out one at a time from
+// a counter in the workspace, each producer fetching its next index while it
+// issues the copies of the current tile.  CTAs that stream faster (SMs
+// differ in how fast their memory requests are served) then take more of
+// the tail, instead of idling while the slowest CTA finishes.  Each stage
+// carries the index of its tile, and a stage with index -1 tells the
+// consumers that their CTA is done.  The last producer to finish leaves the
+// counters at zero for the next launch.
+//
 // Every wait on an mbarrier gives up after a time limit (read from the
-// global timer); the kernel then records the failure in `err` and returns,
-// the producer first waiting (again with a limit) for the copies it issued.
+// global timer); the kernel then records the failure in the error word and
+// returns, the producer first waiting (again with a limit) for the copies it
+// issued.
 #include <atomic>
 #include <mutex>
 
@@ -130,6 +142,18 @@ constexpr int kSlack = 64;
 #endif
 constexpr int kMaxPieces = 32;
 
+// Launches of at least kDynMinRounds rounds of tiles (one tile per CTA a
+// round) hand out the tiles of their last kDynRounds rounds dynamically.
+// Shorter launches stay cyclic to the end: measured, the dynamic tail cost
+// them more than it saved (7M elements x 16 workers: 55.1 -> 56.2 us),
+// while a 62M-element launch gained 357 -> 351 us.
+constexpr int64_t kDynRounds = 2;
+constexpr int64_t kDynMinRounds = 64;
+
+// Bytes at the end of each stage that carry the stage's tile index (a whole
+// 128-byte line, so that every stage starts 128-byte aligned).
+constexpr int kStageHead = 128;
+
 __device__ __forceinline__ int64_t round_down8(int64_t x) { return x & ~(int64_t)7; }
 __device__ __forceinline__ int64_t round_up8(int64_t x) { return (x + 7) & ~(int64_t)7; }
 
@@ -143,26 +167,36 @@ __device__ __forceinline__ int layer_shift(const Tab &tab, int l)
 
 }  // namespace
 
+// ctr: the workspace's 256-byte block of counter words: [1] the error word,
+// [4..5] the 64-bit counter of dynamically handed-out tiles, [6] the count
+// of producers that have finished with it (all zero between launches).
 // drop_tile >= 0 (test hook only, see fc_test_stage_loss): the producer
 // issues no copies for that tile, so the bounded waits on it run out.
 template <class Tab, int WT, int MAXH, bool MIS>
 __global__ void __launch_bounds__(kThreads, 1)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
-                 float *partials, unsigned *err, const int64_t drop_tile,
+                 float *partials, unsigned *ctr, const int64_t drop_tile,
                  const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end)
 {
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
     unsigned char *stages = smem + 128;
+    unsigned *err = ctr + 1;
+    unsigned long long *dyn_next = reinterpret_cast<unsigned long long *>(ctr + 4);
+    unsigned *dyn_done = ctr + 6;
     const int W = WT > 0 ? WT : tab.W;
     const int L = tab.L;
     const int ROW = TT + (MIS ? kSlack : 0);  // elements per worker row
     const size_t gbytes = (size_t)W * ROW * 2;
-    const size_t sbytes = gbytes + (size_t)TT * 4 + (MIS ? kMaxPieces * sizeof(int4) : 0);
+    const size_t sbytes =
+        gbytes + (size_t)TT * 4 + (MIS ? kMaxPieces * sizeof(int4) : 0) + kStageHead;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // tiles of TT fused elements from f_begin (a multiple of 256) to f_end
     const int64_t ntiles = (f_end - f_begin + TT - 1) / TT;
+    const int64_t G_ = gridDim.x;
+    const bool dyn = ntiles / G_ >= kDynMinRounds;
+    const int64_t rounds_static = dyn ? ntiles / G_ - kDynRounds : (ntiles + G_ - 1) / G_;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < S; ++s) {
@@ -180,18 +214,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kConsumerWarps) {
         // producer
         if (lane != 0) return;
-        int it = 0;
-        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
-            const int s = it % S;
-            if (it >= S && !mbar_wait(smem_u32(&bars[S + s]), ((it / S) - 1) & 1, limit_ns)) {
-                atomicOr(err, 1u);
-                break;
-            }
-            if (t == drop_tile) continue;
-            const int64_t f0 = f_begin + t * TT;
-            const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
+        // Fills stage s with tile t (its index first, for the consumers).
+        auto issue = [&](int s, int64_t t) {
             const uint32_t full = smem_u32(&bars[s]);
             unsigned char *st = stages + (size_t)s * sbytes;
+            *reinterpret_cast<volatile int64_t *>(st + sbytes - kStageHead) = t;
+            if (t == drop_tile) return;
+            const int64_t f0 = f_begin + t * TT;
+            const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
             const uint32_t rbytes = resid ? (uint32_t)((f1 - f0) * 4) : 0u;
             if constexpr (!MIS) {
                 mbar_expect_tx(full, (uint32_t)((f1 - f0) * 2 * W) + rbytes);
@@ -257,6 +287,50 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
             if (resid) bulk_g2s(smem_u32(st + gbytes), resid + f0, rbytes, full);
+        };
+        // Waits until the consumers have released the slot of iteration it.
+        auto slot_free = [&](int it) {
+            const int s = it % S;
+            if (it >= S && !mbar_wait(smem_u32(&bars[S + s]), ((it / S) - 1) & 1, limit_ns)) {
+                atomicOr(err, 1u);
+                return false;
+            }
+            return true;
+        };
+        int it = 0;
+        bool ok = true;
+        // the cyclic rounds: kept free of any other work, since the
+        // producer's issue rate bounds the kernel's
+        for (; it < rounds_static; ++it) {
+            const int64_t t = blockIdx.x + (int64_t)it * G_;
+            if (t >= ntiles) break;
+            if (!slot_free(it)) {
+                ok = false;
+                break;
+            }
+            issue(it % S, t);
+        }
+        // the tail, handed out one tile at a time; the next index travels
+        // while this tile's copies go out
+        if (ok && dyn) {
+            unsigned long long q = atomicAdd(dyn_next, 1ull);
+            for (;; ++it) {
+                const int64_t t = rounds_static * G_ + (int64_t)q;
+                if (t >= ntiles) break;
+                if (!slot_free(it)) {
+                    ok = false;
+                    break;
+                }
+                q = atomicAdd(dyn_next, 1ull);
+                issue(it % S, t);
+            }
+        }
+        // no tile left: the consumers stop at this stage
+        if (ok && slot_free(it)) {
+            unsigned char *st = stages + (size_t)(it % S) * sbytes;
+            *reinterpret_cast<volatile int64_t *>(st + sbytes - kStageHead) = -1;
+            mbar_arrive(smem_u32(&bars[it % S]));
+            ++it;
         }
         // No copy may still be landing in shared memory when the CTA exits:
         // wait for every stage still in flight (each wait bounded; a stage
@@ -264,20 +338,30 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = it > S ? it - S : 0; j < it; ++j)
             if (!mbar_wait(smem_u32(&bars[j % S]), (j / S) & 1, limit_ns))
                 atomicOr(err, 2u);
+        // Every index this producer fetched has come back (the fence waits
+        // for its atomics); the last producer to get here resets the counters.
+        if (dyn) {
+            __threadfence();
+            if (atomicAdd(dyn_done, 1u) == gridDim.x - 1) {
+                atomicExch(dyn_next, 0ull);
+                atomicExch(dyn_done, 0u);
+            }
+        }
         return;
     }
 
     // consumers
-    int it = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+    for (int it = 0;; ++it) {
         const int s = it % S;
         if (!mbar_wait(smem_u32(&bars[s]), (it / S) & 1, limit_ns)) {
             if (lane == 0) atomicOr(err, 4u);
             return;
         }
+        const unsigned char *st = stages + (size_t)s * sbytes;
+        const int64_t t = *reinterpret_cast<const volatile int64_t *>(st + sbytes - kStageHead);
+        if (t < 0) break;
         const int64_t f0 = f_begin + t * TT;
         const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
-        const unsigned char *st = stages + (size_t)s * sbytes;
         for (int64_t lo = f0 + (int64_t)warp * FC_UNIT; lo < f1;
              lo += (int64_t)kConsumerWarps * FC_UNIT) {
             const int64_t hi = lo + FC_UNIT < f1 ? lo + FC_UNIT : f1;
@@ -402,7 +486,7 @@ static void tma_shape(int W, bool mis, int &TT, int &S, size_t &smem)
     while (TT > FC_UNIT && (size_t)W * TT * 2 > 65536) TT /= 2;
     const size_t row = (size_t)TT + (mis ? kSlack : 0);
     const size_t sbytes = (size_t)W * row * 2 + (size_t)TT * 4 +
-                          (mis ? kMaxPieces * sizeof(int4) : 0);
+                          (mis ? kMaxPieces * sizeof(int4) : 0) + kStageHead;
     const size_t cap = 227 * 1024 - 128;
     S = (int)(cap / sbytes);
     if (S > 4) S = 4;
@@ -446,7 +530,7 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
 template <class Tab, int WT, int MAXH, bool MIS>
 static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                                 const float *resid, float *out, float *partials,
-                                unsigned *err, cudaStream_t s, int64_t fb, int64_t fe)
+                                unsigned *ctr, cudaStream_t s, int64_t fb, int64_t fe)
 {
     int TT, S;
     size_t smem;
@@ -471,18 +555,18 @@ static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
     const int64_t drop = g_drop_tile.exchange(-1);
     const uint64_t limit = drop >= 0 ? g_drop_limit_ns.load() : kWaitLimitNs;
     return launch_after_prior(kern, (unsigned)grid, kThreads, smem, s, tab, G, TT, S, u,
-                              resid, out, partials, err, drop, limit, fb, fe);
+                              resid, out, partials, ctr, drop, limit, fb, fe);
 }
 
 template <class Tab, bool MIS>
 static cudaError_t launch_tma_layout(const Tab &tab, const UnitGeom &G, float u,
                                      const float *resid, float *out, float *partials,
-                                     unsigned *err, cudaStream_t s, int64_t fb, int64_t fe)
+                                     unsigned *ctr, cudaStream_t s, int64_t fb, int64_t fe)
 {
     switch (tab.W) {
-    case 4: return launch_tma_w<Tab, 4, 3, MIS>(tab, G, u, resid, out, partials, err, s, fb, fe);
-    case 8: return launch_tma_w<Tab, 8, 4, MIS>(tab, G, u, resid, out, partials, err, s, fb, fe);
-    case 16: return launch_tma_w<Tab, 16, 5, MIS>(tab, G, u, resid, out, partials, err, s, fb, fe);
+    case 4: return launch_tma_w<Tab, 4, 3, MIS>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 8: return launch_tma_w<Tab, 8, 4, MIS>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 16: return launch_tma_w<Tab, 16, 5, MIS>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
     default: break;
     }
     return cudaErrorNotSupported;
@@ -491,16 +575,16 @@ static cudaError_t launch_tma_layout(const Tab &tab, const UnitGeom &G, float u,
 template <class Tab>
 cudaError_t launch_reduce_tma(const Tab &tab, const UnitGeom &G, float u,
                               const float *resid, float *out, float *partials,
-                              unsigned *err, cudaStream_t s, int layout, int64_t fb,
+                              unsigned *ctr, cudaStream_t s, int layout, int64_t fb,
                               int64_t fe)
 {
     if (fe < 0) fe = G.N;
     if (fb >= fe) return cudaSuccess;
     if (fb % FC_UNIT != 0) return cudaErrorInvalidValue;
     if (layout == 1)
-        return launch_tma_layout<Tab, false>(tab, G, u, resid, out, partials, err, s, fb, fe);
+        return launch_tma_layout<Tab, false>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
     if (layout == 2)
-        return launch_tma_layout<Tab, true>(tab, G, u, resid, out, partials, err, s, fb, fe);
+        return launch_tma_layout<Tab, true>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
     return cudaErrorNotSupported;
 }
 

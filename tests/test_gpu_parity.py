@@ -634,21 +634,25 @@ def test_layer_group_streaming_waits_for_each_group():
 
 
 def _counter_words(ws, N, chunk):
-    """The first four 32-bit words of the pipeline workspace's counter block
-    (after the fp32 unit sums, at a 256-byte boundary)."""
+    """The first eight 32-bit words of the pipeline workspace's counter block
+    (after the fp32 unit sums, at a 256-byte boundary): the selection's
+    count of finished blocks, the staged reduction's error word, the step's
+    outcome, and the staged reduction's tile counter and finished-producer
+    count."""
     C = -(-N // chunk)
     U = -(-chunk // 256)
     units = (C - 1) * U + -(-(N - (C - 1) * chunk) // 256)
     off = -(-units * 4 // 256) * 256
-    return ws[off: off + 16].cpu().numpy().view(np.uint32)
+    return ws[off: off + 32].cpu().numpy().view(np.uint32)
 
 
 @pytest.mark.parametrize("name", ["googlenet", "tiny", "aligned16"])
 def test_pipeline_leaves_its_counters_at_zero(name):
     """The workspace's counter block (the selection's count of finished
-    blocks, the staged reduction's error word) is zero again after whole
-    steps and after steps streamed per layer group: a workspace zeroed once
-    serves every later step."""
+    blocks, the staged reduction's error word and tile counters, and the
+    outcome of a step that was applied) is zero again after whole steps and
+    after steps streamed per layer group: a workspace zeroed once serves
+    every later step."""
     kw = SPAN_CASES.get(name)
     wl = workload.get(name) if kw is None else workload.custom(config_id=171, steps=1, **kw)
     g = dev_grads(workload.all_grads(wl, 0))
