@@ -2,8 +2,8 @@
 // gradients.
 //
 // FireCaffe (arXiv 1511.00175), §6: the workers' gradient vectors are summed
-// element-wise, through a reduction tree of branching factor 2 and depth
-// log2(p).  GradientFlow (arXiv 1902.06855), abstract: mixed precision
+// element-wise, through a binary reduction tree whose depth is the base-2
+// log of the worker count.  GradientFlow (arXiv 1902.06855), abstract: mixed precision
 // (fp16 gradients, fp32 sums here) and lazy allreduce, which fuses the
 // per-layer operations into one; here the fusion is a layout (offsets) that
 // the reduction reads through, so the fused copy need not be materialised.

@@ -1,7 +1,7 @@
 // a3 chunk norms and a4 top-k chunk selection + compaction.
 //
 // GradientFlow (arXiv 1902.06855), abstract: coarse-grained sparse
-// communication sends only the important gradient chunks.  The pages do not
+// communication sends only the chunks that matter.  The pages do not
 // define importance or how many chunks; the engine scores a chunk by its L2
 // norm and keeps the k chunks that come first in (norm descending, index
 // ascending) order.

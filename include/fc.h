@@ -12,9 +12,9 @@
  *   a2 reduce   element-wise sum over the workers (FireCaffe, "near-linear
  *               acceleration of deep neural network training on compute
  *               clusters", arXiv 1511.00175, §6: allreduce of vectors of
- *               length |dW|) in a binary reduction tree (same §6: branching
- *               factor 2, depth log2(p)), accumulated in fp32 (mixed
- *               precision, GradientFlow abstract) and unscaled by
+ *               length |dW|) in a binary reduction tree (same §6: its depth
+ *               is the base-2 log of the worker count), accumulated in fp32
+ *               (mixed precision, GradientFlow abstract) and unscaled by
  *               1/(loss scale * W)
  *   a3 norms    L2 norm of every fixed-size chunk of the fused vector
  *   a4 select   keep the k highest-norm chunks and compact them (GradientFlow

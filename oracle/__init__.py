@@ -126,8 +126,8 @@ def fuse_pack(grads: List[List[np.ndarray]]) -> np.ndarray:
 # ---- a2: tree reduce --------------------------------------------------------
 
 def tree_sum(x: Sequence[float]) -> np.float32:
-    """Level-order binary-tree sum of float32 values (FireCaffe §6:
-    branching factor 2, depth log2(p))."""
+    """Level-order binary-tree sum of float32 values (FireCaffe §6: a
+    binary reduction tree, depth the base-2 log of the worker count)."""
     a = _c(x, np.float32).copy()
     return np.float32(_load().orc_tree_sum(_ptr(a), len(a)))
 

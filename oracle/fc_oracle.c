@@ -14,14 +14,14 @@
  *  - FireCaffe: near-linear acceleration of deep neural network training on
  *    compute clusters (arXiv 1511.00175).
  *      §6: gradients of the workers are summed element-wise (allreduce over
- *          vectors of length |dW|); reduction trees with branching factor 2
- *          and depth log2(p); the workers apply the summed update.
+ *          vectors of length |dW|) in a binary tree whose depth is the
+ *          base-2 log of the worker count; the workers apply the sum.
  *      §3: batched SGD; Eq. 1 sizes the weight volume.
  *  - Optimizing Network Performance for Distributed DNN Training on GPU
  *    Clusters: ImageNet/AlexNet Training in 1.5 Minutes (GradientFlow,
  *    arXiv 1902.06855), abstract: mixed-precision training; lazy allreduce
  *    fuses many communication operations into one; coarse-grained sparse
- *    communication transmits only important gradient chunks.
+ *    communication sends only the chunks that matter.
  *  The pages leave the score, the selection rule, the residual and the
  *  optimiser open; the readings taken here are: L2 norm of a chunk as its
  *  importance, top-k chunks with ties to the lower index, unkept values
