@@ -626,6 +626,46 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                         velocity, weights, weights_fp16, norms, idx, mask, packed,
                         packed_fp16, send_scale, threshold, &N));
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
+    // small problems: the whole step in one cluster launch
+    if (!stage_loss_armed()) {
+        DeviceScope scope;
+        TRY(scope.bind(a));
+        const WsLayout wl = ws_layout(N, chunk);
+        SmallStep st;
+        st.G = ugeom(N, chunk);
+        st.u = (float)(1.0 / ((double)loss_scale * (double)W));
+        st.resid = residual;
+        st.a = a;
+        st.partials = (float *)((char *)workspace + wl.partials);
+        st.norms = norms;
+        st.k = k;
+        st.idx = idx;
+        st.mask = mask;
+        st.threshold = threshold;
+        st.status = (unsigned *)((char *)workspace + wl.counters) + 2;
+        st.lr = lr;
+        st.mu = momentum;
+        st.r = residual;
+        st.v = velocity;
+        st.w = weights;
+        st.w16 = (__half *)weights_fp16;
+        st.packed = packed;
+        st.packed16 = (__half *)packed_fp16;
+        st.send_scale = send_scale;
+        bool launched = false;
+        cudaError_t e;
+        if (fits_small(W, L)) {
+            TableS tab;
+            fill_table(tab, grads, W, L, sizes);
+            e = launch_step_small(tab, st, (cudaStream_t)stream, false, &launched);
+        } else {
+            static thread_local TableL tab;
+            fill_table(tab, grads, W, L, sizes);
+            e = launch_step_small(tab, st, (cudaStream_t)stream, false, &launched);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "step_small launch");
+        if (launched) return ok();
+    }
     TRY(fc_step_reduce(grads, W, L, sizes, loss_scale, chunk, residual, a,
                        workspace, workspace_bytes, stream));
     TRY(fc_step_select(N, chunk, k, norms, idx, mask, threshold, workspace,
@@ -634,6 +674,35 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                        weights_fp16, mask, packed, packed_fp16, send_scale,
                        workspace, workspace_bytes, stream));
     return ok();
+}
+
+int32_t fc_step_path(const void *const *grads, int32_t W, int32_t L, const int64_t *sizes,
+                     int64_t chunk)
+{
+    int64_t N = 0;
+    if (check_sizes(L, sizes, &N) != FC_OK || check_table(grads, W, L, sizes) != FC_OK)
+        return -1;
+    if (chunk < 1) {
+        fail(FC_ERR_INVALID_ARG, "chunk must be >= 1");
+        return -1;
+    }
+    SmallStep st = {};
+    st.G = ugeom(N, chunk);
+    bool small = false;
+    cudaError_t e;
+    if (fits_small(W, L)) {
+        TableS tab;
+        fill_table(tab, grads, W, L, sizes);
+        e = launch_step_small(tab, st, nullptr, true, &small);
+    } else {
+        static thread_local TableL tab;
+        fill_table(tab, grads, W, L, sizes);
+        e = launch_step_small(tab, st, nullptr, true, &small);
+    }
+    (void)e;
+    (void)cudaGetLastError();
+    ok();
+    return small ? FC_STEP_ONE_LAUNCH : FC_STEP_THREE_KERNELS;
 }
 
 fc_status fc_step_status(const void *workspace, size_t workspace_bytes, int64_t N,

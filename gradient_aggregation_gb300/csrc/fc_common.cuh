@@ -376,4 +376,46 @@ __device__ __forceinline__ float norm_from_sumsq(FF ss)
     return __fsqrt_rn(__fadd_rn(ss.hi, ss.lo));
 }
 
+// Chunk norm from the unit sums, in the fixed order (see the top of this file):
+// lane t adds units t, t+32, ... in float-float arithmetic, then the
+// butterfly.  Called by a whole warp; the result is valid in lane 0.
+// The unit sums are loaded eight per lane at a time, all eight loads in
+// flight before the first addition, so a chunk of up to 256 units costs one
+// memory round trip; the additions keep the order above.
+__device__ __forceinline__ float chunk_norm_from_units(const UnitGeom &G,
+                                                       const float *partials,
+                                                       int64_t c, int lane)
+{
+    const int64_t Uc = units_of_chunk(G, c);
+    const float *p = partials + c * G.U;
+    FF ss = {0.f, 0.f};
+    for (int64_t j0 = lane; j0 < Uc; j0 += 8 * 32) {
+        float x[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+            const int64_t j = j0 + 32 * q;
+            x[q] = j < Uc ? __ldcg(p + j) : 0.f;
+        }
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            if (j0 + 32 * q < Uc) ss = ff_add(ss, x[q]);
+    }
+    return norm_from_sumsq(warp_sum_ff(ss));
+}
+
+// ---- the update -------------------------------------------------------------------
+
+// One element of a5: g = kept ? a : 0, r = kept ? 0 : a, v = mu*v + lr*g as
+// two products and their sum, w = w - v; every operation one rounding.
+__device__ __forceinline__ void sgd1(float a, bool kept, float lr, float mu,
+                                     float &r, float &v, float &w)
+{
+    const float g = kept ? a : 0.f;
+    r = kept ? 0.f : a;
+    const float t1 = __fmul_rn(mu, v);
+    const float t2 = __fmul_rn(lr, g);
+    v = __fadd_rn(t1, t2);
+    w = __fsub_rn(w, v);
+}
+
 }  // namespace fc

@@ -71,6 +71,45 @@ cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           __half *w16, bool inplace, cudaStream_t s,
                           const unsigned *status = nullptr);
 
+// ---- fc_step in one launch (small problems) ------------------------------------
+
+// The one-launch path serves chunk sizes that are multiples of 8, at most
+// FC_SMALL_MAX_CHUNKS chunks, at most FC_SMALL_MAX_N elements, at most 64
+// workers, and at most FC_SMALL_UNITS_PER_WARP 256-element units per warp of
+// the cluster.
+#define FC_SMALL_MAX_CHUNKS 1024
+#define FC_SMALL_MAX_N (1 << 19)
+#define FC_SMALL_UNITS_PER_WARP 8
+
+struct SmallStep {
+    UnitGeom G;
+    float u;                 // binary32 nearest 1/(S*W)
+    const float *resid;      // may be NULL
+    float *a, *partials, *norms;
+    int64_t k;
+    int32_t *idx;
+    uint8_t *mask;
+    float *threshold;
+    unsigned *status;        // the workspace's step-outcome word
+    float lr, mu;
+    float *r, *v, *w;
+    __half *w16;
+    float *packed;
+    __half *packed16;
+    float send_scale;
+};
+
+// Launches the whole step as one cluster kernel when the problem and the
+// device allow it (*ok = true), else launches nothing (*ok = false).  With
+// probe_only, only decides.
+template <class Tab>
+cudaError_t launch_step_small(const Tab &tab, const SmallStep &st, cudaStream_t s,
+                              bool probe_only, bool *ok);
+
+// True while fc_test_stage_loss has armed the next staged launch (fc_step
+// then takes the three-kernel path, whose phase 1 is that launch).
+bool stage_loss_armed();
+
 // Sets the calling thread's fc_last_error() message; returns st.
 fc_status set_error(fc_status st, const char *msg);
 

@@ -601,6 +601,8 @@ extern "C" fc_status fc_test_stage_loss(int64_t tile, uint64_t wait_limit_ns)
 
 namespace fc {
 
+bool stage_loss_armed() { return g_drop_tile.load() >= 0; }
+
 template int tma_layout<TableS>(const TableS &, const UnitGeom &, const float *);
 template int tma_layout<TableL>(const TableL &, const UnitGeom &, const float *);
 template cudaError_t launch_reduce_tma<TableS>(const TableS &, const UnitGeom &, float,

@@ -128,33 +128,6 @@ __device__ __forceinline__ uint64_t block_excl_scan64(uint64_t x, uint64_t *sw,
     return (warp ? sw[warp - 1] : 0ull) + inc - x;
 }
 
-// Chunk norm from the unit sums, in the fixed order (see fc_common.cuh):
-// lane t adds units t, t+32, ... in float-float arithmetic, then the
-// butterfly.  Called by a whole warp; the result is valid in lane 0.
-// The unit sums are loaded eight per lane at a time, all eight loads in
-// flight before the first addition, so a chunk of up to 256 units costs one
-// memory round trip; the additions keep the order above.
-__device__ __forceinline__ float chunk_norm_from_units(const UnitGeom &G,
-                                                       const float *partials,
-                                                       int64_t c, int lane)
-{
-    const int64_t Uc = units_of_chunk(G, c);
-    const float *p = partials + c * G.U;
-    FF ss = {0.f, 0.f};
-    for (int64_t j0 = lane; j0 < Uc; j0 += 8 * 32) {
-        float x[8];
-#pragma unroll
-        for (int q = 0; q < 8; ++q) {
-            const int64_t j = j0 + 32 * q;
-            x[q] = j < Uc ? __ldcg(p + j) : 0.f;
-        }
-#pragma unroll
-        for (int q = 0; q < 8; ++q)
-            if (j0 + 32 * q < Uc) ss = ff_add(ss, x[q]);
-    }
-    return norm_from_sumsq(warp_sum_ff(ss));
-}
-
 // Selection kernel.  With partials != NULL every block first turns the unit
 // sums of 32 chunks (one per warp) into norms; the block that finishes last
 // (a count of finished blocks in `done`, reset by that block) then runs the

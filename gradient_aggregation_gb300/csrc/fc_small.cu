@@ -1,0 +1,434 @@
+// fc_step in one launch for small problems (a few hundred thousand
+// elements): one thread-block cluster runs a2..a5 with hardware cluster
+// barriers between the phases, instead of three kernels.
+//
+// The three-kernel pipeline pays three launches and two full-device
+// hand-offs per step, which bounds a 133K-element step at 17 us whatever
+// the kernels do.  Here the CTAs of one cluster (16 where the GPU allows,
+// else 8) share the work:
+//  1. reduce: warp gw of the cluster takes the 256-element units gw,
+//     gw + nw, ... (nw warps in all) with the tree, unscale and residual of
+//     the register kernel (`k_reduce`), writes `a` and the unit sums of
+//     squares;
+//  2. norms: warp gw finishes the norms of chunks gw, gw + nw, ... from the
+//     unit sums in the fixed float-float order of the selection kernel, and
+//     writes each norm's bit pattern into the shared memory of every CTA of
+//     the cluster (distributed shared memory);
+//  3. select: every chunk's rank in (norm descending, index ascending)
+//     order is counted against all C keys, which each CTA holds; the chunk
+//     of rank k-1 gives the threshold tau and its index c_tau, sent to
+//     every CTA.  Chunk c is kept iff key_c > tau, or key_c == tau and
+//     c <= c_tau: exactly the k chunks first in that order, the same set the
+//     radix select of the pipeline finds;
+//  4. update: warp gw updates its own units again (re-reading the `a` it
+//     wrote), with each kept chunk's send-buffer slot counted from the keys
+//     (kept chunks before it), exactly as the update kernel does.
+// Every sum and product is the same binary32 operation in the same order
+// as in the three kernels, so the results are the same bits (the GPU tests
+// compare both paths and the oracle).  The cluster barriers are hardware
+// barriers (barrier.cluster with release/acquire at cluster scope): no CTA
+// spins, and no CTA ever waits for anything outside its cluster.
+#include <mutex>
+
+#include "fc_internal.h"
+
+namespace fc {
+
+namespace {
+
+constexpr int kSmallThreads = 512;
+constexpr int kSmallWarps = kSmallThreads / 32;
+
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+__device__ __forceinline__ uint32_t cluster_size()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster arrives; memory operations
+// before the barrier (shared, distributed shared and global) are visible to
+// every thread of the cluster after it.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile(
+        "barrier.cluster.arrive.release.aligned;\n\t"
+        "barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Stores v at the address of `local` (a shared variable) in CTA `rank` of
+// the cluster.
+__device__ __forceinline__ void st_cluster_u32(const void *local, uint32_t rank, uint32_t v)
+{
+    const uint32_t a = (uint32_t)__cvta_generic_to_shared(local);
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(rank));
+    asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(r), "r"(v) : "memory");
+}
+
+// Chunk c is kept iff it comes before the k-th chunk (tau, c_tau) in
+// (key descending, index ascending) order, or is that chunk.
+__device__ __forceinline__ bool is_kept(uint32_t key, int64_t c, uint32_t tau, int64_t ctau)
+{
+    return key > tau || (key == tau && c <= ctau);
+}
+
+}  // namespace
+
+struct SmallArgs {
+    UnitGeom G;
+    float u;
+    const float *resid;
+    float *a;
+    float *partials;
+    float *norms;
+    int64_t k;
+    int32_t *idx;
+    uint8_t *mask;
+    float *threshold;
+    unsigned *status;
+    float lr, mu;
+    float *r, *v, *w;
+    __half *w16;
+    float *packed;
+    __half *packed16;
+    float send_scale;
+    int inplace;
+};
+
+template <class Tab, int WT, int MAXH>
+__global__ void __launch_bounds__(kSmallThreads, 1)
+    k_step_small(const __grid_constant__ Tab tab, const SmallArgs A)
+{
+    // the chunks' keys (norm bit patterns), padded with zeros to a multiple
+    // of 4, and the k-th chunk
+    __shared__ __align__(16) uint32_t skeys[FC_SMALL_MAX_CHUNKS + 4];
+    __shared__ uint32_t s_tau, s_ctau;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const uint32_t crank = cluster_rank(), ncta = cluster_size();
+    const int64_t gw = (int64_t)crank * kSmallWarps + warp;
+    const int64_t nw = (int64_t)ncta * kSmallWarps;
+    const UnitGeom &G = A.G;
+    const int64_t C = G.C;
+    const int W = WT > 0 ? WT : tab.W;
+    const int L = tab.L;
+    const uint64_t pol = policy_evict_first();
+    // Launched after whatever the stream ran before (programmatic
+    // serialisation): no global memory is touched before that work is done.
+    wait_for_prior_grid();
+    allow_dependent_launch();
+    if (threadIdx.x < 4) skeys[C + threadIdx.x] = 0u;
+
+    // ---- 1. reduce (the register kernel's arithmetic; chunk sizes are
+    // multiples of 8, so a unit has at most 32 groups of 8: one per lane)
+    for (int64_t un = gw; un < G.units; un += nw) {
+        int64_t c, lo, hi;
+        unit_range(G, un, c, lo, hi);
+        const int64_t f0 = lo + 8 * (int64_t)lane;
+        float tss = 0.f;
+        if (f0 < hi) {
+            float a[8];
+            int l = find_layer(tab, f0);
+            if (f0 + 8 <= hi && f0 + 8 <= tab.off[l + 1] && ((tab.vec[l >> 5] >> (l & 31)) & 1u)) {
+                const int64_t j = f0 - tab.off[l];
+                tree_sum<WT, MAXH, 8>(
+                    W,
+                    [&](int wk, float(&x)[8]) {
+                        unpack8(ld_stream16(tab.ptr[wk * L + l] + j, pol), x);
+                    },
+                    a);
+                float r[8];
+                if (A.resid) {
+                    const float4 r0 = __ldcs(reinterpret_cast<const float4 *>(A.resid + f0));
+                    const float4 r1 = __ldcs(reinterpret_cast<const float4 *>(A.resid + f0 + 4));
+                    r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
+                    r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
+                }
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    a[e] = __fmul_rn(a[e], A.u);
+                    if (A.resid) a[e] = __fadd_rn(a[e], r[e]);
+                }
+                reinterpret_cast<float4 *>(A.a + f0)[0] = make_float4(a[0], a[1], a[2], a[3]);
+                reinterpret_cast<float4 *>(A.a + f0)[1] = make_float4(a[4], a[5], a[6], a[7]);
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    const int64_t f = f0 + e;
+                    if (f >= hi) {
+                        a[e] = 0.f;
+                        continue;
+                    }
+                    while (tab.off[l + 1] <= f) ++l;
+                    const int64_t j = f - tab.off[l];
+                    float s1[1];
+                    tree_sum<WT, MAXH, 1>(
+                        W,
+                        [&](int wk, float(&x)[1]) {
+                            x[0] = ld_half_as_float(tab.ptr[wk * L + l] + j);
+                        },
+                        s1);
+                    float val = __fmul_rn(s1[0], A.u);
+                    if (A.resid) val = __fadd_rn(val, __ldcs(A.resid + f));
+                    A.a[f] = val;
+                    a[e] = val;
+                }
+            }
+            tss = __fadd_rn(tss, group_sumsq(a));
+        }
+        tss = warp_sum_f32(tss);
+        if (lane == 0) A.partials[un] = tss;
+    }
+    cluster_sync();
+
+    // ---- 2. norms, and every norm's key into every CTA's shared memory
+    for (int64_t c = gw; c < C; c += nw) {
+        const float n = chunk_norm_from_units(G, A.partials, c, lane);
+        const uint32_t key = __shfl_sync(0xffffffffu, __float_as_uint(n), 0);
+        if (lane == 0) A.norms[c] = n;
+        if ((uint32_t)lane < ncta) st_cluster_u32(&skeys[c], (uint32_t)lane, key);
+    }
+    cluster_sync();
+
+    // ---- 3. select: the chunk of rank k-1 (CTA r ranks chunks r*per ...)
+    {
+        const int64_t per = (C + ncta - 1) / ncta;
+        const int64_t c = (int64_t)crank * per + threadIdx.x;
+        if (threadIdx.x < per && c < C) {
+            const uint32_t kc = skeys[c];
+            uint32_t above = 0;
+            // keys past C are 0: never above, never equal with a lower index
+            for (int64_t j4 = 0; j4 < C; j4 += 4) {
+                const uint4 q = *reinterpret_cast<const uint4 *>(&skeys[j4]);
+                above += (q.x > kc || (q.x == kc && j4 < c)) ? 1u : 0u;
+                above += (q.y > kc || (q.y == kc && j4 + 1 < c)) ? 1u : 0u;
+                above += (q.z > kc || (q.z == kc && j4 + 2 < c)) ? 1u : 0u;
+                above += (q.w > kc || (q.w == kc && j4 + 3 < c)) ? 1u : 0u;
+            }
+            if ((int64_t)above == A.k - 1) {
+                for (uint32_t t = 0; t < ncta; ++t) {
+                    st_cluster_u32(&s_tau, t, kc);
+                    st_cluster_u32(&s_ctau, t, (uint32_t)c);
+                }
+                A.threshold[0] = __uint_as_float(kc);
+                if (A.status) *A.status = 0u;  // the step is applied
+            }
+        }
+    }
+    cluster_sync();
+
+    // ---- 4. update, unit by unit as in step 1
+    const uint32_t tau = s_tau;
+    const int64_t ctau = s_ctau;
+    const int64_t cs = G.cs;
+    for (int64_t un = gw; un < G.units; un += nw) {
+        int64_t c, lo, hi;
+        unit_range(G, un, c, lo, hi);
+        const bool kept = is_kept(skeys[c], c, tau, ctau);
+        // slot of chunk c in the send buffers: kept chunks before it
+        uint32_t slot = 0;
+        if (kept) {
+            for (int64_t j = lane; j < c; j += 32) slot += is_kept(skeys[j], j, tau, ctau) ? 1u : 0u;
+            slot = __reduce_add_sync(0xffffffffu, slot);
+        }
+        if (lo == c * cs && lane == 0) {
+            A.mask[c] = kept ? 1 : 0;
+            if (kept) A.idx[slot] = (int32_t)c;
+        }
+        const bool pk = kept && (A.packed != nullptr || A.packed16 != nullptr);
+        const int64_t pbase = pk ? (int64_t)slot * cs - c * cs : 0;
+        const bool need_a = kept || !A.inplace;
+        const int64_t f0 = lo + 8 * (int64_t)lane;
+        if (f0 < hi) {
+            if (f0 + 8 <= hi) {
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    const int64_t i0 = f0 + 4 * h;
+                    float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
+                    if (need_a) av = *reinterpret_cast<const float4 *>(A.a + i0);  // this thread's own step-1 writes
+                    float4 vv = __ldcs(reinterpret_cast<const float4 *>(A.v + i0));
+                    float4 ww = __ldcs(reinterpret_cast<const float4 *>(A.w + i0));
+                    float4 rr;
+                    sgd1(av.x, kept, A.lr, A.mu, rr.x, vv.x, ww.x);
+                    sgd1(av.y, kept, A.lr, A.mu, rr.y, vv.y, ww.y);
+                    sgd1(av.z, kept, A.lr, A.mu, rr.z, vv.z, ww.z);
+                    sgd1(av.w, kept, A.lr, A.mu, rr.w, vv.w, ww.w);
+                    __stcs(reinterpret_cast<float4 *>(A.v + i0), vv);
+                    __stcs(reinterpret_cast<float4 *>(A.w + i0), ww);
+                    if (need_a) __stcs(reinterpret_cast<float4 *>(A.r + i0), rr);
+                    if (A.w16) {
+                        __half2 h0 = __floats2half2_rn(ww.x, ww.y);
+                        __half2 h1 = __floats2half2_rn(ww.z, ww.w);
+                        uint2 hv;
+                        hv.x = *reinterpret_cast<uint32_t *>(&h0);
+                        hv.y = *reinterpret_cast<uint32_t *>(&h1);
+                        __stcs(reinterpret_cast<uint2 *>(A.w16 + i0), hv);
+                    }
+                    if (pk && A.packed) __stcs(reinterpret_cast<float4 *>(A.packed + pbase + i0), av);
+                    if (pk && A.packed16) {
+                        const __half2 s0 = __floats2half2_rn(__fmul_rn(av.x, A.send_scale),
+                                                             __fmul_rn(av.y, A.send_scale));
+                        const __half2 s1 = __floats2half2_rn(__fmul_rn(av.z, A.send_scale),
+                                                             __fmul_rn(av.w, A.send_scale));
+                        uint2 hv;
+                        hv.x = *reinterpret_cast<const uint32_t *>(&s0);
+                        hv.y = *reinterpret_cast<const uint32_t *>(&s1);
+                        __stcs(reinterpret_cast<uint2 *>(A.packed16 + pbase + i0), hv);
+                    }
+                }
+            } else {
+                for (int64_t i = f0; i < hi; ++i) {
+                    const float ai = need_a ? A.a[i] : 0.f;
+                    float vi = A.v[i], wi = A.w[i], ri;
+                    sgd1(ai, kept, A.lr, A.mu, ri, vi, wi);
+                    A.v[i] = vi;
+                    A.w[i] = wi;
+                    if (need_a) A.r[i] = ri;
+                    if (A.w16) A.w16[i] = __float2half_rn(wi);
+                    if (pk && A.packed) A.packed[pbase + i] = ai;
+                    if (pk && A.packed16)
+                        A.packed16[pbase + i] = __float2half_rn(__fmul_rn(ai, A.send_scale));
+                }
+            }
+        }
+        // the short last chunk: zero its send-buffer slot past N
+        if (pk && hi == G.N) {
+            for (int64_t i = G.N + lane; i < c * cs + cs; i += 32) {
+                if (A.packed) A.packed[pbase + i] = 0.f;
+                if (A.packed16) A.packed16[pbase + i] = __float2half_rn(0.f);
+            }
+        }
+    }
+}
+
+namespace {
+
+// Cluster size per (kernel, device): 16 CTAs where the GPU schedules such a
+// cluster of this kernel, else 8, else 0 (one-launch path unavailable).
+int cluster_ctas(const void *kern, int dev)
+{
+    struct Entry {
+        const void *kern;
+        int dev, ctas;
+    };
+    static std::mutex mu;
+    static Entry cache[64];
+    static int used = 0;
+    std::lock_guard<std::mutex> lock(mu);
+    for (int i = 0; i < used; ++i)
+        if (cache[i].kern == kern && cache[i].dev == dev) return cache[i].ctas;
+    int ctas = 0;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+        cudaSuccess)
+        (void)cudaGetLastError();
+    for (int n : {16, 8}) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(n);
+        cfg.blockDim = dim3(kSmallThreads);
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = n;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int clusters = 0;
+        if (cudaOccupancyMaxActiveClusters(&clusters, kern, &cfg) == cudaSuccess && clusters >= 1) {
+            ctas = n;
+            break;
+        }
+        (void)cudaGetLastError();
+    }
+    if (used < 64) cache[used++] = Entry{kern, dev, ctas};
+    return ctas;
+}
+
+template <class Tab, int WT, int MAXH>
+cudaError_t launch_small_w(const Tab &tab, const SmallArgs &args, cudaStream_t s, bool probe_only,
+                           bool *ok)
+{
+    auto kern = k_step_small<Tab, WT, MAXH>;
+    int dev = 0;
+    cudaGetDevice(&dev);
+    const int ctas = cluster_ctas((const void *)kern, dev);
+    // units are taken one per warp and round
+    const int64_t max_units = (int64_t)ctas * kSmallWarps * FC_SMALL_UNITS_PER_WARP;
+    *ok = ctas > 0 && args.G.units <= max_units;
+    if (probe_only || !*ok) return cudaSuccess;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(ctas);
+    cfg.blockDim = dim3(kSmallThreads);
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = ctas;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, kern, tab, args);
+}
+
+}  // namespace
+
+template <class Tab>
+cudaError_t launch_step_small(const Tab &tab, const SmallStep &st, cudaStream_t s,
+                              bool probe_only, bool *ok)
+{
+    *ok = false;
+    const UnitGeom &G = st.G;
+    if (G.cs % 8 != 0 || G.C > FC_SMALL_MAX_CHUNKS || G.N > FC_SMALL_MAX_N || tab.W > 64)
+        return cudaSuccess;
+    SmallArgs A;
+    A.G = G;
+    A.u = st.u;
+    A.resid = st.resid;
+    A.a = st.a;
+    A.partials = st.partials;
+    A.norms = st.norms;
+    A.k = st.k;
+    A.idx = st.idx;
+    A.mask = st.mask;
+    A.threshold = st.threshold;
+    A.status = st.status;
+    A.lr = st.lr;
+    A.mu = st.mu;
+    A.r = st.r;
+    A.v = st.v;
+    A.w = st.w;
+    A.w16 = st.w16;
+    A.packed = st.packed;
+    A.packed16 = st.packed16;
+    A.send_scale = st.send_scale;
+    A.inplace = st.a == st.r ? 1 : 0;
+#define FC_S(WT, MAXH) launch_small_w<Tab, WT, MAXH>(tab, A, s, probe_only, ok)
+    switch (tab.W) {
+    case 1: return FC_S(1, 1);
+    case 2: return FC_S(2, 2);
+    case 4: return FC_S(4, 3);
+    case 8: return FC_S(8, 4);
+    case 16: return FC_S(16, 5);
+    case 32: return FC_S(32, 6);
+    case 64: return FC_S(64, 7);
+    default: break;
+    }
+    if (tab.W < 32) return FC_S(0, 5);
+    return FC_S(0, 7);
+#undef FC_S
+}
+
+template cudaError_t launch_step_small<TableS>(const TableS &, const SmallStep &, cudaStream_t,
+                                               bool, bool *);
+template cudaError_t launch_step_small<TableL>(const TableL &, const SmallStep &, cudaStream_t,
+                                               bool, bool *);
+
+}  // namespace fc

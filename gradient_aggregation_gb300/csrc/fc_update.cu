@@ -20,17 +20,6 @@
 
 namespace fc {
 
-__device__ __forceinline__ void sgd1(float a, bool kept, float lr, float mu,
-                                     float &r, float &v, float &w)
-{
-    const float g = kept ? a : 0.f;
-    r = kept ? 0.f : a;
-    const float t1 = __fmul_rn(mu, v);
-    const float t2 = __fmul_rn(lr, g);
-    v = __fadd_rn(t1, t2);
-    w = __fsub_rn(w, v);
-}
-
 // Threads per block of the update (each tile of 2048 elements is 512
 // 16-byte groups, spread over the block's threads).
 #ifndef FC_UPDATE_BLOCK

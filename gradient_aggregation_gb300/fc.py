@@ -31,6 +31,7 @@ FC_MAX_TABLE_LAYERS = 512
 FC_NOALLOC_WORKSPACE_BYTES = 4 << 20
 FC_ORDER_TREE, FC_ORDER_SEQUENTIAL, FC_ORDER_RING = 0, 1, 2
 FC_REDUCE_REGISTER, FC_REDUCE_STAGED, FC_REDUCE_STAGED_SHIFTED = 0, 1, 2
+FC_STEP_THREE_KERNELS, FC_STEP_ONE_LAUNCH = 0, 1
 
 _lock = threading.Lock()
 _lib = None
@@ -49,6 +50,7 @@ _SIGS = {
     "fc_step_reduce_ordered": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _I32,
                                               _P, _SZ, _P]),
     "fc_step_reduce_kernel": (_I32, [_P, _I32, _I32, _P, _I64, _I32]),
+    "fc_step_path": (_I32, [_P, _I32, _I32, _P, _I64]),
     "fc_step_reduce_span": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _I64, _I64,
                                            _P, _SZ, _P]),
     "fc_unit_start": (_I64, [_I64, _I64, _I64]),
@@ -313,6 +315,16 @@ def fc_step_reduce_kernel(grads, chunk: int, order: int = FC_ORDER_TREE) -> int:
     PtrTable.from_addresses can build from plain addresses)."""
     t = _table(grads)
     r = int(lib().fc_step_reduce_kernel(t.ptrs, t.W, t.L, t.sizes_c, int(chunk), int(order)))
+    if r < 0:
+        _check(FC_ERR_INVALID_ARG)
+    return r
+
+
+def fc_step_path(grads, chunk: int) -> int:
+    """FC_STEP_* of how fc_step runs this layout on the current device
+    (one cluster launch for small problems, else three kernels)."""
+    t = _table(grads)
+    r = int(lib().fc_step_path(t.ptrs, t.W, t.L, t.sizes_c, int(chunk)))
     if r < 0:
         _check(FC_ERR_INVALID_ARG)
     return r

@@ -363,7 +363,10 @@ FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk,
 FC_API fc_status fc_step_status(const void *workspace, size_t workspace_bytes,
                                 int64_t N, int64_t chunk, void *stream);
 
-/* Phases 1-3 in one call on one stream (three kernel launches). */
+/* Phases 1-3 in one call on one stream.  Small problems run as one launch
+ * of one thread-block cluster (see fc_step_path); all others as the three
+ * kernels of fc_step_reduce, fc_step_select and fc_step_update.  Both give
+ * the same bits. */
 FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                          const int64_t *sizes, float loss_scale, int64_t chunk,
                          int64_t k, float lr, float momentum, float *residual,
@@ -372,6 +375,25 @@ FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                          uint8_t *mask, float *packed, void *packed_fp16,
                          float send_scale, float *threshold, void *workspace,
                          size_t workspace_bytes, void *stream);
+
+/* How fc_step runs a problem of this layout on the current device:
+ *  FC_STEP_THREE_KERNELS  the three kernels of fc_step_reduce,
+ *                         fc_step_select and fc_step_update;
+ *  FC_STEP_ONE_LAUNCH     one launch of one thread-block cluster (16 CTAs
+ *                         where the GPU can schedule them, else 8) that runs
+ *                         all three phases with hardware cluster barriers
+ *                         between them.  It serves chunk sizes that are
+ *                         multiples of 8, up to 1024 chunks, up to 2^19
+ *                         elements, up to 64 workers, and up to 8
+ *                         256-element units per warp of the cluster.
+ * Returns -1 for arguments fc_step would reject.  Queries the device (the
+ * cluster occupancy) on its first call per device; without a device the
+ * answer is FC_STEP_THREE_KERNELS.  While fc_test_stage_loss is armed,
+ * fc_step takes the three kernels whatever this returns. */
+#define FC_STEP_THREE_KERNELS 0
+#define FC_STEP_ONE_LAUNCH 1
+FC_API int32_t fc_step_path(const void *const *grads, int32_t W, int32_t L,
+                            const int64_t *sizes, int64_t chunk);
 
 /* ---- the pipeline without a caller workspace ---------------------------------- */
 

@@ -69,6 +69,16 @@ class GpuRun:
                        self.residual, self.a, self.velocity, self.weights, self.w16,
                        self.norms, self.idx, self.mask, self.packed, self.threshold,
                        self.ws, stream, self.packed16, self.send_scale)
+        elif self.path == "phases":
+            # the pipeline's three kernels called one by one (never the
+            # one-launch path)
+            fc.fc_step_reduce(grads_dev, wl.loss_scale, wl.chunk, self.residual, self.a,
+                              self.ws, stream)
+            fc.fc_step_select(self.N, wl.chunk, self.k, self.norms, self.idx, self.mask,
+                              self.threshold, self.ws, stream)
+            fc.fc_step_update(self.a, self.N, wl.chunk, wl.lr, wl.momentum, self.residual,
+                              self.velocity, self.weights, self.w16, self.mask, self.packed,
+                              self.ws, self.packed16, self.send_scale, stream)
         else:
             self.offsets = fc.fc_fuse_pack(grads_dev, self.fused, stream)
             fc.fc_tree_reduce(self.fused, wl.W, self.N, wl.loss_scale, self.residual,

@@ -819,3 +819,81 @@ def test_engines_on_several_host_threads_match_sequential_runs():
         wa, wb = _engine_bits(a), _engine_bits(b)
         for k in wa:
             assert bits_equal(wa[k], wb[k]), k
+
+
+# ---- fc_step in one cluster launch (small problems) ---------------------------------
+
+ONE_LAUNCH_CASES = {
+    "tiny": None,
+    "w1": dict(W=1, sizes=[3000, 17], chunk=256, keep_percent=10),
+    "w3_ragged": dict(W=3, sizes=[1234, 7], chunk=104, keep_percent=50),
+    "w5": dict(W=5, sizes=[1001, 64, 3333, 2, 700], chunk=304, keep_percent=30),
+    "w7_keep_all": dict(W=7, sizes=[5000, 33, 12000], chunk=1000, keep_percent=100),
+    "w16_shifted": dict(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512, keep_percent=25),
+    "w16_one_chunk": dict(W=16, sizes=[4096, 808, 8, 6000], chunk=16384, keep_percent=10),
+    "w64": dict(W=64, sizes=[40000], chunk=256, keep_percent=10),
+    "w8_chunk8": dict(W=8, sizes=[7000, 1], chunk=8, keep_percent=1),
+    "w16_many_chunks": dict(W=16, sizes=[262144], chunk=256, keep_percent=37),
+}
+
+
+@pytest.mark.parametrize("inplace", [False, True], ids=["separate_a", "inplace"])
+@pytest.mark.parametrize("name", list(ONE_LAUNCH_CASES))
+def test_one_launch_step_matches_three_kernels_and_the_oracle(name, inplace):
+    """Small problems run fc_step as one launch of one thread-block cluster.
+    Its results, over two steps with state carried, are the bits of the
+    three pipeline kernels called one by one and match the oracle element by
+    element (send buffers and fp16 weights included)."""
+    kw = ONE_LAUNCH_CASES[name]
+    wl = workload.get(name) if kw is None else workload.custom(config_id=500, steps=2, **kw)
+    one = GpuRun(wl, "pipeline", inplace=inplace)
+    three = GpuRun(wl, "phases", inplace=inplace)
+    st = oracle.State(workload.initial_weights(wl))
+    for s in range(2):
+        g_np = workload.all_grads(wl, s)
+        g = dev_grads(g_np)
+        assert fc.fc_step_path(g, wl.chunk) == fc.FC_STEP_ONE_LAUNCH
+        one.step(g)
+        three.step(g)
+        a, b = one.snapshot(), three.snapshot()
+        _compare_paths(a, b)
+        oracle_step(g_np, st, wl, a)
+        assert fc.fc_step_status(one.ws, one.N, wl.chunk) == fc.FC_OK
+
+
+def test_one_launch_step_with_ties_and_misaligned_pointers():
+    """All-equal norms (ties keep the lowest indices) and gradient pointers
+    shifted differently per worker (the element path), in one launch."""
+    wl = workload.custom(W=4, sizes=[2048, 2048], chunk=256, keep_percent=25,
+                         config_id=510, steps=1)
+    g_np = [[np.full(n, 0.5, np.float16) for n in wl.sizes] for _ in range(wl.W)]
+    one = GpuRun(wl, "pipeline")
+    st = oracle.State(workload.initial_weights(wl))
+    out = []
+    for w, row in enumerate(g_np):
+        r = []
+        for g in row:
+            buf = torch.empty(g.size + 8, dtype=torch.float16, device="cuda")
+            view = buf[1 + w % 3: 1 + w % 3 + g.size]
+            view.copy_(torch.from_numpy(g))
+            r.append(view)
+        out.append(r)
+    assert fc.fc_step_path(out, wl.chunk) == fc.FC_STEP_ONE_LAUNCH
+    one.step(out)
+    snap = one.snapshot()
+    assert list(snap["idx"]) == list(range(one.k))
+    oracle_step(g_np, st, wl, snap)
+
+
+def test_step_path_choice():
+    """The one-launch path needs chunk sizes that are multiples of 8 and a
+    small problem; the rest take the three kernels."""
+    small = dev_grads(workload.all_grads(workload.custom(W=4, sizes=[4096], chunk=256,
+                                                          keep_percent=10, config_id=520,
+                                                          steps=1), 0))
+    assert fc.fc_step_path(small, 256) == fc.FC_STEP_ONE_LAUNCH
+    assert fc.fc_step_path(small, 100) == fc.FC_STEP_THREE_KERNELS      # chunk % 8 != 0
+    assert fc.fc_step_path(small, 12) == fc.FC_STEP_THREE_KERNELS       # chunk % 8 != 0
+    assert fc.fc_step_path(small, 8) == fc.FC_STEP_ONE_LAUNCH           # 512 chunks
+    big = fc.PtrTable.from_addresses([[1 << 20], [2 << 20]], [1 << 20])
+    assert fc.fc_step_path(big, 4096) == fc.FC_STEP_THREE_KERNELS       # 2^20 elements
