@@ -444,8 +444,18 @@ def run_gpu(args, wl, rank, world, local):
                     wl.momentum, torch.from_numpy(workload.initial_weights(wl)).to(dev))
     s = torch.cuda.Stream(device=dev)
     phases = list(eng.phases(table, s))
+    # Small problems run fc_step as one cluster launch: the timed step is
+    # then that one kernel, and its events bracket the whole step.
+    one_launch = fc.fc_step_path(table, wl.chunk) == fc.FC_STEP_ONE_LAUNCH
 
     def step_phased(evs=None):
+        if one_launch:
+            if evs is not None:
+                evs[0].record(s)
+            eng.step(table, s)
+            if evs is not None:
+                evs[1].record(s)
+            return
         if evs is not None:
             evs[0].record(s)
         phases[0]()
@@ -502,7 +512,7 @@ def run_gpu(args, wl, rank, world, local):
     # roofline of the dominant kernel (phase 1: tree reduce + norm partials)
     C = -(-N // wl.chunk)
     alg = step_algorithmic_bytes(wl, eng.k)
-    k_alg = alg["phase1"]
+    k_alg = alg["step"] if one_launch else alg["phase1"]
     k_ms = statistics.mean(reduce_ms)
 
     # the same phase-1 kernel launched back to back on its own (out of place,
@@ -510,15 +520,19 @@ def run_gpu(args, wl, rank, world, local):
     iso = None
     try:
         a_tmp = torch.empty(N, dtype=torch.float32, device=dev)
+        def once():
+            if one_launch:
+                eng.step(table, s)
+            else:
+                fc.fc_step_reduce(table, wl.loss_scale, wl.chunk, eng.residual, a_tmp,
+                                  eng.workspace, s)
         for _ in range(3):
-            fc.fc_step_reduce(table, wl.loss_scale, wl.chunk, eng.residual, a_tmp,
-                              eng.workspace, s)
+            once()
         i0, i1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         KI = max(MIN_PHASE1, min(K, 200))
         i0.record(s)
         for _ in range(KI):
-            fc.fc_step_reduce(table, wl.loss_scale, wl.chunk, eng.residual, a_tmp,
-                              eng.workspace, s)
+            once()
         i1.record(s)
         torch.cuda.synchronize()
         iso_ms = i0.elapsed_time(i1) / KI
@@ -797,9 +811,15 @@ def run_gpu(args, wl, rank, world, local):
             "dtype": "f32", "data": "synthetic (seeded Gaussian fp16 gradients, workload-shaped)",
             "config": config_of(wl, {
                 "parallelism": "replicas" if world > 1 else "single GPU",
-                "path": "fc_step: pack-elided tree reduce + norm partials, radix top-k select, "
-                        "residual/momentum-SGD update with packed kept chunks (3 kernels)",
-                "l2": "inputs larger than L2: %.2f GB fp16 gradients + %.2f GB fp32 state per step"
+                "path": ("fc_step in one cluster launch: tree reduce + norms, ranked top-k "
+                         "select, residual/momentum-SGD update with packed kept chunks"
+                         if one_launch else
+                         "fc_step: pack-elided tree reduce + norm partials, radix top-k select, "
+                         "residual/momentum-SGD update with packed kept chunks (3 kernels)"),
+                "l2": ("inputs larger than L2: %.2f GB fp16 gradients + %.2f GB fp32 state per "
+                       "step" if step_bytes + 12 * N > 129e6 else
+                       "inputs smaller than L2 (%.4f GB fp16 gradients + %.4f GB fp32 state): "
+                       "the step runs from L2, a latency-bound size")
                       % (step_bytes / 1e9, 12 * N / 1e9)}),
             "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                          "unit": "GB/s", "frac": round(achieved / peak, 4),
@@ -809,7 +829,9 @@ def run_gpu(args, wl, rank, world, local):
                                             "profiles/k_reduce_%s.md taken on this kernel "
                                             "source (not measured in this run)" % wl.name)
                                            if traffic is not None else None,
-                         "kernel": "phase 1 of fc_step (%s)" % phase1_kernel(wl, table),
+                         "kernel": ("k_step_small: the whole fc_step in one cluster launch"
+                                    if one_launch else
+                                    "phase 1 of fc_step (%s)" % phase1_kernel(wl, table)),
                          "algorithmic_bytes_per_launch": k_alg,
                          "avg_launch_ms": round(k_ms, 5),
                          "median_launch_ms": round(statistics.median(reduce_ms), 5),
@@ -828,7 +850,7 @@ def run_gpu(args, wl, rank, world, local):
             "e2e": e2e,
             "graph": graph,
             "materialised_pack": mat,
-            "gpu_launches": 3 * K,
+            "gpu_launches": (1 if one_launch else 3) * K,
             "clocks": clocks,
         }
         print(json.dumps(line), flush=True)

@@ -36,8 +36,6 @@ namespace fc {
 
 namespace {
 
-constexpr int kSmallThreads = 512;
-constexpr int kSmallWarps = kSmallThreads / 32;
 
 __device__ __forceinline__ uint32_t cluster_rank()
 {
@@ -103,14 +101,19 @@ struct SmallArgs {
     int inplace;
 };
 
-template <class Tab, int WT, int MAXH>
-__global__ void __launch_bounds__(kSmallThreads, 1)
+// NT threads per CTA: 1024 for up to 4 workers (the tree then fits in 64
+// registers a thread), else 512.
+template <class Tab, int WT, int MAXH, int NT>
+__global__ void __launch_bounds__(NT, 1)
     k_step_small(const __grid_constant__ Tab tab, const SmallArgs A)
 {
+    constexpr int kSmallWarps = NT / 32;
     // the chunks' keys (norm bit patterns), padded with zeros to a multiple
-    // of 4, and the k-th chunk
+    // of 4; the k-th chunk; the kept chunks as a bitmask and the number of
+    // kept chunks before each 32-chunk word
     __shared__ __align__(16) uint32_t skeys[FC_SMALL_MAX_CHUNKS + 4];
     __shared__ uint32_t s_tau, s_ctau;
+    __shared__ uint32_t s_kept[FC_SMALL_MAX_CHUNKS / 32], s_before[FC_SMALL_MAX_CHUNKS / 32];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const uint32_t crank = cluster_rank(), ncta = cluster_size();
     const int64_t gw = (int64_t)crank * kSmallWarps + warp;
@@ -119,15 +122,23 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const int64_t C = G.C;
     const int W = WT > 0 ? WT : tab.W;
     const int L = tab.L;
-    const uint64_t pol = policy_evict_first();
+    // Every CTA of the cluster must be running before any writes to another
+    // one's shared memory: arrive now, wait once the work ahead in the
+    // stream is done (by then every CTA has arrived).
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
     // Launched after whatever the stream ran before (programmatic
     // serialisation): no global memory is touched before that work is done.
     wait_for_prior_grid();
     allow_dependent_launch();
+    asm volatile("barrier.cluster.wait.aligned;" ::: "memory");
     if (threadIdx.x < 4) skeys[C + threadIdx.x] = 0u;
 
     // ---- 1. reduce (the register kernel's arithmetic; chunk sizes are
-    // multiples of 8, so a unit has at most 32 groups of 8: one per lane)
+    // multiples of 8, so a unit has at most 32 groups of 8: one per lane).
+    // With one unit per chunk (chunks of at most 256 elements) the warp that
+    // reduced a unit also finishes its chunk's norm (step 2) at once: lane 0
+    // holds the chunk's only unit sum and the float-float butterfly is the
+    // one of step 2, so the bits are the same.
     for (int64_t un = gw; un < G.units; un += nw) {
         int64_t c, lo, hi;
         unit_range(G, un, c, lo, hi);
@@ -141,7 +152,7 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                 tree_sum<WT, MAXH, 8>(
                     W,
                     [&](int wk, float(&x)[8]) {
-                        unpack8(ld_stream16(tab.ptr[wk * L + l] + j, pol), x);
+                        unpack8(__ldg(reinterpret_cast<const uint4 *>(tab.ptr[wk * L + l] + j)), x);
                     },
                     a);
                 float r[8];
@@ -185,38 +196,72 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
         }
         tss = warp_sum_f32(tss);
         if (lane == 0) A.partials[un] = tss;
+        if (G.U == 1) {
+            FF ss = {0.f, 0.f};
+            if (lane == 0) ss = ff_add(ss, tss);
+            const float n = norm_from_sumsq(warp_sum_ff(ss));
+            const uint32_t key = __shfl_sync(0xffffffffu, __float_as_uint(n), 0);
+            if (lane == 0) A.norms[c] = n;
+            if ((uint32_t)lane < ncta) st_cluster_u32(&skeys[c], (uint32_t)lane, key);
+        }
     }
-    cluster_sync();
 
-    // ---- 2. norms, and every norm's key into every CTA's shared memory
-    for (int64_t c = gw; c < C; c += nw) {
-        const float n = chunk_norm_from_units(G, A.partials, c, lane);
-        const uint32_t key = __shfl_sync(0xffffffffu, __float_as_uint(n), 0);
-        if (lane == 0) A.norms[c] = n;
-        if ((uint32_t)lane < ncta) st_cluster_u32(&skeys[c], (uint32_t)lane, key);
-    }
-    cluster_sync();
-
-    // ---- 3. select: the chunk of rank k-1 (CTA r ranks chunks r*per ...)
-    {
-        const int64_t per = (C + ncta - 1) / ncta;
-        const int64_t c = (int64_t)crank * per + threadIdx.x;
-        if (threadIdx.x < per && c < C) {
-            const uint32_t kc = skeys[c];
-            uint32_t above = 0;
-            // keys past C are 0: never above, never equal with a lower index
-            for (int64_t j4 = 0; j4 < C; j4 += 4) {
-                const uint4 q = *reinterpret_cast<const uint4 *>(&skeys[j4]);
-                above += (q.x > kc || (q.x == kc && j4 < c)) ? 1u : 0u;
-                above += (q.y > kc || (q.y == kc && j4 + 1 < c)) ? 1u : 0u;
-                above += (q.z > kc || (q.z == kc && j4 + 2 < c)) ? 1u : 0u;
-                above += (q.w > kc || (q.w == kc && j4 + 3 < c)) ? 1u : 0u;
+    // ---- 2. norms, and every norm's key into every CTA's shared memory.
+    // Up to four of this warp's chunks at a time have all their unit sums
+    // in flight before the first addition; the additions follow the fixed
+    // order (lane t: units t, t+32, ... in float-float, then the butterfly).
+    if (G.U > 1) cluster_sync();
+    for (int64_t c0 = gw; c0 < C && G.U > 1; c0 += 4 * nw) {
+        float x[4][8];
+        int64_t Uc[4];
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t c = c0 + q * nw;
+            Uc[q] = c < C ? units_of_chunk(G, c) : 0;
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const int64_t jj = lane + 32 * i;
+                x[q][i] = jj < Uc[q] ? __ldcg(A.partials + c * G.U + jj) : 0.f;
             }
-            if ((int64_t)above == A.k - 1) {
-                for (uint32_t t = 0; t < ncta; ++t) {
-                    st_cluster_u32(&s_tau, t, kc);
-                    st_cluster_u32(&s_ctau, t, (uint32_t)c);
-                }
+        }
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+            const int64_t c = c0 + q * nw;
+            if (c >= C) break;
+            float n;
+            if (Uc[q] <= 256) {
+                FF ss = {0.f, 0.f};
+#pragma unroll
+                for (int i = 0; i < 8; ++i)
+                    if (lane + 32 * i < Uc[q]) ss = ff_add(ss, x[q][i]);
+                n = norm_from_sumsq(warp_sum_ff(ss));
+            } else {
+                n = chunk_norm_from_units(G, A.partials, c, lane);
+            }
+            const uint32_t key = __shfl_sync(0xffffffffu, __float_as_uint(n), 0);
+            if (lane == 0) A.norms[c] = n;
+            if ((uint32_t)lane < ncta) st_cluster_u32(&skeys[c], (uint32_t)lane, key);
+        }
+    }
+    cluster_sync();
+
+    // ---- 3. select: the chunk of rank k-1.  Warp gw ranks chunks gw,
+    // gw + nw, ...: lane t counts the chunks j = t, t+32, ... before it in
+    // (key descending, index ascending) order.
+    for (int64_t c = gw; c < C; c += nw) {
+        const uint32_t kc = skeys[c];
+        uint32_t above = 0;
+        for (int64_t j = lane; j < C; j += 32) {
+            const uint32_t kj = skeys[j];
+            above += (kj > kc || (kj == kc && j < c)) ? 1u : 0u;
+        }
+        above = __reduce_add_sync(0xffffffffu, above);
+        if ((int64_t)above == A.k - 1) {
+            if ((uint32_t)lane < ncta) {
+                st_cluster_u32(&s_tau, (uint32_t)lane, kc);
+                st_cluster_u32(&s_ctau, (uint32_t)lane, (uint32_t)c);
+            }
+            if (lane == 0) {
                 A.threshold[0] = __uint_as_float(kc);
                 if (A.status) *A.status = 0u;  // the step is applied
             }
@@ -228,16 +273,32 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
     const uint32_t tau = s_tau;
     const int64_t ctau = s_ctau;
     const int64_t cs = G.cs;
+    // the kept chunks as a bitmask, and the kept chunks before each word
+    const int64_t nwords = (C + 31) / 32;
+    for (int64_t wd = warp; wd < nwords; wd += kSmallWarps) {
+        const int64_t c = 32 * wd + lane;
+        const uint32_t bits = __ballot_sync(0xffffffffu, c < C && is_kept(skeys[c], c, tau, ctau));
+        if (lane == 0) s_kept[wd] = bits;
+    }
+    __syncthreads();
+    if (warp == 0) {
+        const uint32_t cnt = lane < nwords ? (uint32_t)__popc(s_kept[lane]) : 0u;
+        uint32_t inc = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += y;
+        }
+        if (lane < nwords) s_before[lane] = inc - cnt;
+    }
+    __syncthreads();
     for (int64_t un = gw; un < G.units; un += nw) {
         int64_t c, lo, hi;
         unit_range(G, un, c, lo, hi);
-        const bool kept = is_kept(skeys[c], c, tau, ctau);
+        const uint32_t word = s_kept[c >> 5];
+        const bool kept = (word >> (c & 31)) & 1u;
         // slot of chunk c in the send buffers: kept chunks before it
-        uint32_t slot = 0;
-        if (kept) {
-            for (int64_t j = lane; j < c; j += 32) slot += is_kept(skeys[j], j, tau, ctau) ? 1u : 0u;
-            slot = __reduce_add_sync(0xffffffffu, slot);
-        }
+        const uint32_t slot = s_before[c >> 5] + (uint32_t)__popc(word & ((1u << (c & 31)) - 1u));
         if (lo == c * cs && lane == 0) {
             A.mask[c] = kept ? 1 : 0;
             if (kept) A.idx[slot] = (int32_t)c;
@@ -253,8 +314,8 @@ __global__ void __launch_bounds__(kSmallThreads, 1)
                     const int64_t i0 = f0 + 4 * h;
                     float4 av = make_float4(0.f, 0.f, 0.f, 0.f);
                     if (need_a) av = *reinterpret_cast<const float4 *>(A.a + i0);  // this thread's own step-1 writes
-                    float4 vv = __ldcs(reinterpret_cast<const float4 *>(A.v + i0));
-                    float4 ww = __ldcs(reinterpret_cast<const float4 *>(A.w + i0));
+                    float4 vv = *reinterpret_cast<const float4 *>(A.v + i0);
+                    float4 ww = *reinterpret_cast<const float4 *>(A.w + i0);
                     float4 rr;
                     sgd1(av.x, kept, A.lr, A.mu, rr.x, vv.x, ww.x);
                     sgd1(av.y, kept, A.lr, A.mu, rr.y, vv.y, ww.y);
@@ -312,7 +373,7 @@ namespace {
 
 // Cluster size per (kernel, device): 16 CTAs where the GPU schedules such a
 // cluster of this kernel, else 8, else 0 (one-launch path unavailable).
-int cluster_ctas(const void *kern, int dev)
+int cluster_ctas(const void *kern, int dev, int threads)
 {
     struct Entry {
         const void *kern;
@@ -331,7 +392,7 @@ int cluster_ctas(const void *kern, int dev)
     for (int n : {16, 8}) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3(n);
-        cfg.blockDim = dim3(kSmallThreads);
+        cfg.blockDim = dim3(threads);
         cudaLaunchAttribute attr[1];
         attr[0].id = cudaLaunchAttributeClusterDimension;
         attr[0].val.clusterDim.x = n;
@@ -354,17 +415,19 @@ template <class Tab, int WT, int MAXH>
 cudaError_t launch_small_w(const Tab &tab, const SmallArgs &args, cudaStream_t s, bool probe_only,
                            bool *ok)
 {
-    auto kern = k_step_small<Tab, WT, MAXH>;
+    constexpr int NT = (WT > 0 && WT <= 4) ? 1024 : 512;
+    constexpr int kSmallWarps = NT / 32;
+    auto kern = k_step_small<Tab, WT, MAXH, NT>;
     int dev = 0;
     cudaGetDevice(&dev);
-    const int ctas = cluster_ctas((const void *)kern, dev);
+    const int ctas = cluster_ctas((const void *)kern, dev, NT);
     // units are taken one per warp and round
     const int64_t max_units = (int64_t)ctas * kSmallWarps * FC_SMALL_UNITS_PER_WARP;
     *ok = ctas > 0 && args.G.units <= max_units;
     if (probe_only || !*ok) return cudaSuccess;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(ctas);
-    cfg.blockDim = dim3(kSmallThreads);
+    cfg.blockDim = dim3(NT);
     cfg.stream = s;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
