@@ -207,15 +207,37 @@ def test_fused_buffer_with_ragged_rows():
 
 
 def test_ties_keep_lowest_indices():
-    """Every chunk has the same norm: the k lowest chunk indices are kept."""
+    """Every chunk has the same norm: the k lowest chunk indices are kept, by
+    the one-launch step, the three pipeline kernels and the five calls."""
     W, N, cs = 4, 64 * 10, 64
     wl = workload.custom(W=W, sizes=[N], chunk=cs, keep_percent=30, config_id=152)
     g = [[np.full(N, 2.0, dtype=np.float16)] for _ in range(W)]
-    for path in ("pipeline", "separate"):
+    for path in ("pipeline", "phases", "separate"):
         run = GpuRun(wl, path)
         run.step(dev_grads(g))
         snap = run.snapshot()
         assert list(snap["idx"]) == [0, 1, 2]
+        oracle_step(g, oracle.State(workload.initial_weights(wl)), wl, snap)
+
+
+@pytest.mark.parametrize("C", [40, 1000, 5000])
+def test_threshold_inside_a_group_of_ties(C):
+    """Every fifth chunk is large, all others share one smaller norm, and
+    the k-th chunk falls among the equal ones: the large chunks and the
+    lowest-indexed equal ones are kept, on every path."""
+    W, cs = 4, 64
+    wl = workload.custom(W=W, sizes=[C * cs], chunk=cs, keep_percent=30, config_id=153)
+    vals = np.where(np.arange(C) % 5 == 0, 4.0, 1.0).astype(np.float16)
+    g = [[np.repeat(vals, cs)] for _ in range(W)]
+    k = fc.fc_keep_count(C, 30, 100)
+    big = [c for c in range(C) if c % 5 == 0]
+    rest = [c for c in range(C) if c % 5][: k - len(big)]
+    want = sorted(big + rest)
+    for path in ("pipeline", "phases", "separate"):
+        run = GpuRun(wl, path)
+        run.step(dev_grads(g))
+        snap = run.snapshot()
+        assert list(snap["idx"]) == want, path
         oracle_step(g, oracle.State(workload.initial_weights(wl)), wl, snap)
 
 
