@@ -57,6 +57,9 @@ def parse():
     p.add_argument("--no-cpu-baseline", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=10.0,
                    help="target CPU time of the oracle baseline sample")
+    p.add_argument("--phase1-every", type=int, default=0,
+                   help="bracket phase 1 with events on every n-th timed step "
+                        "(default: one in eight, more often on short runs)")
     return p.parse_args()
 
 
@@ -469,7 +472,7 @@ def run_gpu(args, wl, rank, world, local):
     # that at least MIN_PHASE1 launches are timed at any step count: an event
     # between two kernels stops the next one from being scheduled early
     # (programmatic dependent launch), so long runs time one step in eight.
-    EVERY = phase1_every(K)
+    EVERY = args.phase1_every if args.phase1_every > 0 else phase1_every(K)
     evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
            if i % EVERY == 0 else None for i in range(K)]
     start, end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
