@@ -145,9 +145,11 @@ constexpr int kMaxPieces = 32;
 // Launches of at least kDynMinRounds rounds of tiles (one tile per CTA a
 // round) hand out the tiles of their last kDynRounds rounds dynamically.
 // Shorter launches stay cyclic to the end: measured, the dynamic tail cost
-// them more than it saved (7M elements x 16 workers: 55.1 -> 56.2 us),
-// while a 62M-element launch gained 357 -> 351 us.
-constexpr int64_t kDynRounds = 2;
+// them more than it saved (7M elements x 16 workers: 55.1 -> 56.2 us with
+// two rounds; no gain with 2 to 6 rounds once the first index is fetched
+// early), while a 62M-element step gained 525 -> 518 us going from two
+// dynamic rounds to eight.
+constexpr int64_t kDynRounds = 8;
 constexpr int64_t kDynMinRounds = 64;
 
 // Bytes at the end of each stage that carry the stage's tile index (a whole
@@ -299,6 +301,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         };
         int it = 0;
         bool ok = true;
+        unsigned long long q = 0;
         // the cyclic rounds: kept free of any other work, since the
         // producer's issue rate bounds the kernel's
         for (; it < rounds_static; ++it) {
@@ -308,12 +311,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ok = false;
                 break;
             }
+            // the first tail index travels while the last cyclic tile's
+            // copies go out
+            if (dyn && it == rounds_static - 1) q = atomicAdd(dyn_next, 1ull);
             issue(it % S, t);
         }
         // the tail, handed out one tile at a time; the next index travels
         // while this tile's copies go out
         if (ok && dyn) {
-            unsigned long long q = atomicAdd(dyn_next, 1ull);
             for (;; ++it) {
                 const int64_t t = rounds_static * G_ + (int64_t)q;
                 if (t >= ntiles) break;
