@@ -447,9 +447,13 @@ def run_gpu(args, wl, rank, world, local):
                     wl.momentum, torch.from_numpy(workload.initial_weights(wl)).to(dev))
     s = torch.cuda.Stream(device=dev)
     phases = list(eng.phases(table, s))
-    # Small problems run fc_step as one cluster launch: the timed step is
-    # then that one kernel, and its events bracket the whole step.
-    one_launch = fc.fc_step_path(table, wl.chunk) == fc.FC_STEP_ONE_LAUNCH
+    # Small problems run fc_step as one launch: the timed step is then that
+    # one kernel, and its events bracket the whole step.
+    path = fc.fc_step_path(table, wl.chunk)
+    one_launch = path in (fc.FC_STEP_ONE_LAUNCH, fc.FC_STEP_ONE_CLUSTER)
+    one_kernel = ("k_step_grid: the whole fc_step in one cooperative launch, one CTA per SM"
+                  if path == fc.FC_STEP_ONE_LAUNCH else
+                  "k_step_small: the whole fc_step in one thread-block cluster launch")
 
     def step_phased(evs=None):
         if one_launch:
@@ -814,8 +818,10 @@ def run_gpu(args, wl, rank, world, local):
             "dtype": "f32", "data": "synthetic (seeded Gaussian fp16 gradients, workload-shaped)",
             "config": config_of(wl, {
                 "parallelism": "replicas" if world > 1 else "single GPU",
-                "path": ("fc_step in one cluster launch: tree reduce + norms, ranked top-k "
+                "path": ("fc_step in one launch (%s): tree reduce + norms, ranked top-k "
                          "select, residual/momentum-SGD update with packed kept chunks"
+                         % ("cooperative, every SM" if path == fc.FC_STEP_ONE_LAUNCH
+                            else "one cluster")
                          if one_launch else
                          "fc_step: pack-elided tree reduce + norm partials, radix top-k select, "
                          "residual/momentum-SGD update with packed kept chunks (3 kernels)"),
@@ -832,8 +838,7 @@ def run_gpu(args, wl, rank, world, local):
                                             "profiles/k_reduce_%s.md taken on this kernel "
                                             "source (not measured in this run)" % wl.name)
                                            if traffic is not None else None,
-                         "kernel": ("k_step_small: the whole fc_step in one cluster launch"
-                                    if one_launch else
+                         "kernel": (one_kernel if one_launch else
                                     "phase 1 of fc_step (%s)" % phase1_kernel(wl, table)),
                          "algorithmic_bytes_per_launch": k_alg,
                          "avg_launch_ms": round(k_ms, 5),

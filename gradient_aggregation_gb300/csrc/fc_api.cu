@@ -77,8 +77,9 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // 32-bit words (0: the selection's count of finished blocks; 1: the staged
 // reduction's failure word; 2: the last step's outcome, 0 = applied; 4-5:
 // the staged reduction's 64-bit counter of dynamically handed-out tiles; 6:
-// its count of finished producers; all but word 2 zero between calls) and
-// the kept-slot map (int32 [C]).
+// its count of finished producers; all but word 2 zero between calls;
+// 8-12: the one-launch grid step's barrier count and generation and its
+// hand-off of the k-th chunk) and the kept-slot map (int32 [C]).
 struct WsLayout {
     size_t partials, counters, slot, total;
 };
@@ -626,7 +627,7 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                         velocity, weights, weights_fp16, norms, idx, mask, packed,
                         packed_fp16, send_scale, threshold, &N));
     TRY(check_ws(N, chunk, workspace, workspace_bytes));
-    // small problems: the whole step in one cluster launch
+    // small problems: the whole step in one launch
     if (!stage_loss_armed()) {
         DeviceScope scope;
         TRY(scope.bind(a));
@@ -643,6 +644,7 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
         st.mask = mask;
         st.threshold = threshold;
         st.status = (unsigned *)((char *)workspace + wl.counters) + 2;
+        st.bar = (unsigned *)((char *)workspace + wl.counters) + 8;
         st.lr = lr;
         st.mu = momentum;
         st.r = residual;
@@ -652,7 +654,7 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
         st.packed = packed;
         st.packed16 = (__half *)packed_fp16;
         st.send_scale = send_scale;
-        bool launched = false;
+        int launched = FC_STEP_THREE_KERNELS;
         cudaError_t e;
         if (fits_small(W, L)) {
             TableS tab;
@@ -664,7 +666,7 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
             e = launch_step_small(tab, st, (cudaStream_t)stream, false, &launched);
         }
         if (e != cudaSuccess) return cuda_fail(e, "step_small launch");
-        if (launched) return ok();
+        if (launched != FC_STEP_THREE_KERNELS) return ok();
     }
     TRY(fc_step_reduce(grads, W, L, sizes, loss_scale, chunk, residual, a,
                        workspace, workspace_bytes, stream));
@@ -688,7 +690,9 @@ int32_t fc_step_path(const void *const *grads, int32_t W, int32_t L, const int64
     }
     SmallStep st = {};
     st.G = ugeom(N, chunk);
-    bool small = false;
+    static unsigned probe_bar[5];  // never touched: the probe launches nothing
+    st.bar = probe_bar;
+    int small = FC_STEP_THREE_KERNELS;
     cudaError_t e;
     if (fits_small(W, L)) {
         TableS tab;
@@ -702,7 +706,7 @@ int32_t fc_step_path(const void *const *grads, int32_t W, int32_t L, const int64
     (void)e;
     (void)cudaGetLastError();
     ok();
-    return small ? FC_STEP_ONE_LAUNCH : FC_STEP_THREE_KERNELS;
+    return small;
 }
 
 fc_status fc_step_status(const void *workspace, size_t workspace_bytes, int64_t N,

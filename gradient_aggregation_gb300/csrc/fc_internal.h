@@ -97,14 +97,19 @@ struct SmallStep {
     float *packed;
     __half *packed16;
     float send_scale;
+    unsigned *bar;           // five workspace words for the grid kernel (barrier
+                             // count, generation, the k-th chunk and its tag);
+                             // NULL: cluster kernel only
 };
 
-// Launches the whole step as one cluster kernel when the problem and the
-// device allow it (*ok = true), else launches nothing (*ok = false).  With
-// probe_only, only decides.
+// Launches the whole step as one kernel when the problem and the device
+// allow it: a cooperative launch over every SM when st.bar is set and the
+// device runs cooperative launches (*kind = FC_STEP_ONE_LAUNCH), else one
+// thread-block cluster (FC_STEP_ONE_CLUSTER); otherwise launches nothing
+// (FC_STEP_THREE_KERNELS).  With probe_only, only decides.
 template <class Tab>
 cudaError_t launch_step_small(const Tab &tab, const SmallStep &st, cudaStream_t s,
-                              bool probe_only, bool *ok);
+                              bool probe_only, int *kind);
 
 // True while fc_test_stage_loss has armed the next staged launch (fc_step
 // then takes the three-kernel path, whose phase 1 is that launch).

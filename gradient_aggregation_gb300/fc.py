@@ -31,7 +31,7 @@ FC_MAX_TABLE_LAYERS = 512
 FC_NOALLOC_WORKSPACE_BYTES = 4 << 20
 FC_ORDER_TREE, FC_ORDER_SEQUENTIAL, FC_ORDER_RING = 0, 1, 2
 FC_REDUCE_REGISTER, FC_REDUCE_STAGED, FC_REDUCE_STAGED_SHIFTED = 0, 1, 2
-FC_STEP_THREE_KERNELS, FC_STEP_ONE_LAUNCH = 0, 1
+FC_STEP_THREE_KERNELS, FC_STEP_ONE_LAUNCH, FC_STEP_ONE_CLUSTER = 0, 1, 2
 
 _lock = threading.Lock()
 _lib = None
@@ -62,6 +62,8 @@ _SIGS = {
     "fc_chunk_select_workspace": (_SZ, [_I64]),
     "fc_step_status": (ctypes.c_int, [_P, _SZ, _I64, _I64, _P]),
     "fc_test_stage_loss": (ctypes.c_int, [_I64, ctypes.c_uint64]),
+    "fc_test_one_launch_kind": (ctypes.c_int, [_I32]),
+    "fc_test_barrier_loss": (ctypes.c_int, [_I32, ctypes.c_uint64]),
     "fc_step_reduce": (ctypes.c_int, [_P, _I32, _I32, _P, _F32, _I64, _P, _P, _P, _SZ, _P]),
     "fc_step_select": (ctypes.c_int, [_I64, _I64, _I64, _P, _P, _P, _P, _P, _SZ, _P]),
     "fc_step_update": (ctypes.c_int, [_P, _I64, _I64, _F32, _F32, _P, _P, _P, _P, _P, _P, _P,
@@ -204,6 +206,19 @@ def fc_test_stage_loss(tile: int, wait_limit_ns: int = 20_000_000) -> None:
     _check(lib().fc_test_stage_loss(int(tile), int(wait_limit_ns)))
 
 
+def fc_test_one_launch_kind(kind: int) -> None:
+    """Test hook: FC_STEP_ONE_CLUSTER forces the cluster form of the
+    one-launch step, FC_STEP_ONE_LAUNCH restores the default."""
+    _check(lib().fc_test_one_launch_kind(int(kind)))
+
+
+def fc_test_barrier_loss(cta: int, wait_limit_ns: int = 20_000_000) -> None:
+    """Test hook: in the next cooperative one-launch step CTA `cta` skips the
+    grid barrier and the others wait at most wait_limit_ns (see
+    include/fc.h)."""
+    _check(lib().fc_test_barrier_loss(int(cta), int(wait_limit_ns)))
+
+
 # ---- the five calls ---------------------------------------------------------------
 
 def fc_fuse_pack(grads, fused: torch.Tensor, stream=None) -> List[int]:
@@ -322,7 +337,8 @@ def fc_step_reduce_kernel(grads, chunk: int, order: int = FC_ORDER_TREE) -> int:
 
 def fc_step_path(grads, chunk: int) -> int:
     """FC_STEP_* of how fc_step runs this layout on the current device
-    (one cluster launch for small problems, else three kernels)."""
+    (one launch for small problems: cooperative over every SM, or one
+    thread-block cluster; else three kernels)."""
     t = _table(grads)
     r = int(lib().fc_step_path(t.ptrs, t.W, t.L, t.sizes_c, int(chunk)))
     if r < 0:

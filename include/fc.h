@@ -358,15 +358,19 @@ FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk,
  *                  unchanged too, so the step can simply be run again; in
  *                  place (a == residual) phase 1 had already overwritten the
  *                  residual with a for the tiles it reduced, so restore the
- *                  residual before running the step again.
+ *                  residual before running the step again.  The same status
+ *                  comes from a one-launch step (FC_STEP_ONE_LAUNCH) whose
+ *                  grid barrier wait ran out: nothing but `a`, the norms and
+ *                  the unit sums was written, and the barrier's words are
+ *                  left mid-way, so zero the workspace again (as before its
+ *                  first use) before the next step.
  * Other statuses: bad arguments or a failed CUDA call. */
 FC_API fc_status fc_step_status(const void *workspace, size_t workspace_bytes,
                                 int64_t N, int64_t chunk, void *stream);
 
 /* Phases 1-3 in one call on one stream.  Small problems run as one launch
- * of one thread-block cluster (see fc_step_path); all others as the three
- * kernels of fc_step_reduce, fc_step_select and fc_step_update.  Both give
- * the same bits. */
+ * (see fc_step_path); all others as the three kernels of fc_step_reduce,
+ * fc_step_select and fc_step_update.  All give the same bits. */
 FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                          const int64_t *sizes, float loss_scale, int64_t chunk,
                          int64_t k, float lr, float momentum, float *residual,
@@ -379,19 +383,24 @@ FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
 /* How fc_step runs a problem of this layout on the current device:
  *  FC_STEP_THREE_KERNELS  the three kernels of fc_step_reduce,
  *                         fc_step_select and fc_step_update;
- *  FC_STEP_ONE_LAUNCH     one launch of one thread-block cluster (16 CTAs
- *                         where the GPU can schedule them, else 8) that runs
- *                         all three phases with hardware cluster barriers
- *                         between them.  It serves chunk sizes that are
- *                         multiples of 8, up to 1024 chunks, up to 2^19
- *                         elements, up to 64 workers, and up to 8
- *                         256-element units per warp of the cluster.
- * Returns -1 for arguments fc_step would reject.  Queries the device (the
- * cluster occupancy) on its first call per device; without a device the
- * answer is FC_STEP_THREE_KERNELS.  While fc_test_stage_loss is armed,
- * fc_step takes the three kernels whatever this returns. */
+ *  FC_STEP_ONE_LAUNCH     one cooperative launch with one CTA per SM that
+ *                         runs all three phases, with a grid barrier in the
+ *                         workspace after the norms (bounded waits) and the
+ *                         k-th chunk handed to every CTA through one word;
+ *  FC_STEP_ONE_CLUSTER    where the device runs no cooperative launch: one
+ *                         launch of one thread-block cluster (16 CTAs where
+ *                         the GPU can schedule them, else 8) with hardware
+ *                         cluster barriers between the phases.
+ * The one-launch forms serve chunk sizes that are multiples of 8, up to
+ * 1024 chunks, up to 2^19 elements, up to 64 workers, and up to 8
+ * 256-element units per warp.  Returns -1 for arguments fc_step would
+ * reject.  Queries the device (occupancy, cooperative launch) on its first
+ * call per device; without a device the answer is FC_STEP_THREE_KERNELS.
+ * While fc_test_stage_loss is armed, fc_step takes the three kernels
+ * whatever this returns. */
 #define FC_STEP_THREE_KERNELS 0
 #define FC_STEP_ONE_LAUNCH 1
+#define FC_STEP_ONE_CLUSTER 2
 FC_API int32_t fc_step_path(const void *const *grads, int32_t W, int32_t L,
                             const int64_t *sizes, int64_t chunk);
 
@@ -451,6 +460,22 @@ FC_API fc_status fc_step_noalloc(const void *const *grads, int32_t W,
  * so the following steps run normally.  tile < 0 disarms the hook.  Host
  * only; the next launch from any thread consumes it. */
 FC_API fc_status fc_test_stage_loss(int64_t tile, uint64_t wait_limit_ns);
+
+/* Test hooks for the one-launch step (not part of the method).
+ * fc_test_one_launch_kind(FC_STEP_ONE_CLUSTER) makes fc_step and
+ * fc_step_path use the cluster form even where the cooperative one runs;
+ * FC_STEP_ONE_LAUNCH restores the default.  Other values:
+ * FC_ERR_INVALID_ARG.  Process-wide, host only. */
+FC_API fc_status fc_test_one_launch_kind(int32_t kind);
+
+/* Arms the next cooperative one-launch step: CTA `cta` (clamped to the
+ * last) gives up before the grid barrier, and the other CTAs wait for it at
+ * most wait_limit_ns (0 < limit <= 10 s) instead of 2 s.  Their waits then
+ * run out and the step is not applied: fc_step_status reports
+ * FC_ERR_TIMEOUT, and the workspace must be zeroed again before the next
+ * step.  cta < 0 disarms.  Host only; the next such launch from any thread
+ * consumes it. */
+FC_API fc_status fc_test_barrier_loss(int32_t cta, uint64_t wait_limit_ns);
 
 #ifdef __cplusplus
 }

@@ -843,7 +843,22 @@ def test_engines_on_several_host_threads_match_sequential_runs():
             assert bits_equal(wa[k], wb[k]), k
 
 
-# ---- fc_step in one cluster launch (small problems) ---------------------------------
+# ---- fc_step in one launch (small problems) ------------------------------------------
+
+ONE_LAUNCH_KINDS = {"grid": fc.FC_STEP_ONE_LAUNCH, "cluster": fc.FC_STEP_ONE_CLUSTER}
+
+
+@pytest.fixture(params=list(ONE_LAUNCH_KINDS))
+def one_launch_kind(request):
+    """Runs the test with the cooperative (every SM) and with the cluster
+    form of the one-launch step."""
+    kind = ONE_LAUNCH_KINDS[request.param]
+    fc.fc_test_one_launch_kind(kind)
+    try:
+        yield kind
+    finally:
+        fc.fc_test_one_launch_kind(fc.FC_STEP_ONE_LAUNCH)
+
 
 ONE_LAUNCH_CASES = {
     "tiny": None,
@@ -861,11 +876,12 @@ ONE_LAUNCH_CASES = {
 
 @pytest.mark.parametrize("inplace", [False, True], ids=["separate_a", "inplace"])
 @pytest.mark.parametrize("name", list(ONE_LAUNCH_CASES))
-def test_one_launch_step_matches_three_kernels_and_the_oracle(name, inplace):
-    """Small problems run fc_step as one launch of one thread-block cluster.
-    Its results, over two steps with state carried, are the bits of the
-    three pipeline kernels called one by one and match the oracle element by
-    element (send buffers and fp16 weights included)."""
+def test_one_launch_step_matches_three_kernels_and_the_oracle(name, inplace, one_launch_kind):
+    """Small problems run fc_step as one launch: cooperative over every SM,
+    or one thread-block cluster.  Its results, over two steps with state
+    carried, are the bits of the three pipeline kernels called one by one
+    and match the oracle element by element (send buffers and fp16 weights
+    included)."""
     kw = ONE_LAUNCH_CASES[name]
     wl = workload.get(name) if kw is None else workload.custom(config_id=500, steps=2, **kw)
     one = GpuRun(wl, "pipeline", inplace=inplace)
@@ -874,7 +890,7 @@ def test_one_launch_step_matches_three_kernels_and_the_oracle(name, inplace):
     for s in range(2):
         g_np = workload.all_grads(wl, s)
         g = dev_grads(g_np)
-        assert fc.fc_step_path(g, wl.chunk) == fc.FC_STEP_ONE_LAUNCH
+        assert fc.fc_step_path(g, wl.chunk) == one_launch_kind
         one.step(g)
         three.step(g)
         a, b = one.snapshot(), three.snapshot()
@@ -883,7 +899,7 @@ def test_one_launch_step_matches_three_kernels_and_the_oracle(name, inplace):
         assert fc.fc_step_status(one.ws, one.N, wl.chunk) == fc.FC_OK
 
 
-def test_one_launch_step_with_ties_and_misaligned_pointers():
+def test_one_launch_step_with_ties_and_misaligned_pointers(one_launch_kind):
     """All-equal norms (ties keep the lowest indices) and gradient pointers
     shifted differently per worker (the element path), in one launch."""
     wl = workload.custom(W=4, sizes=[2048, 2048], chunk=256, keep_percent=25,
@@ -900,7 +916,7 @@ def test_one_launch_step_with_ties_and_misaligned_pointers():
             view.copy_(torch.from_numpy(g))
             r.append(view)
         out.append(r)
-    assert fc.fc_step_path(out, wl.chunk) == fc.FC_STEP_ONE_LAUNCH
+    assert fc.fc_step_path(out, wl.chunk) == one_launch_kind
     one.step(out)
     snap = one.snapshot()
     assert list(snap["idx"]) == list(range(one.k))
@@ -919,3 +935,51 @@ def test_step_path_choice():
     assert fc.fc_step_path(small, 8) == fc.FC_STEP_ONE_LAUNCH           # 512 chunks
     big = fc.PtrTable.from_addresses([[1 << 20], [2 << 20]], [1 << 20])
     assert fc.fc_step_path(big, 4096) == fc.FC_STEP_THREE_KERNELS       # 2^20 elements
+    # the cluster form, where a device runs no cooperative launch
+    fc.fc_test_one_launch_kind(fc.FC_STEP_ONE_CLUSTER)
+    try:
+        assert fc.fc_step_path(small, 256) == fc.FC_STEP_ONE_CLUSTER
+        assert fc.fc_step_path(small, 100) == fc.FC_STEP_THREE_KERNELS
+    finally:
+        fc.fc_test_one_launch_kind(fc.FC_STEP_ONE_LAUNCH)
+    with pytest.raises(fc.FcError):
+        fc.fc_test_one_launch_kind(fc.FC_STEP_THREE_KERNELS)
+
+
+@pytest.mark.parametrize("inplace", [False, True], ids=["separate_a", "inplace"])
+def test_one_launch_barrier_wait_runs_out(inplace):
+    """Failure path of the cooperative one-launch step, without any fault:
+    the test hook makes one CTA give up before the grid barrier, so every
+    other CTA's wait runs out (20 ms limit).  The step reports FC_ERR_TIMEOUT
+    and is not applied: velocity, weights, the fp16 weights, the send
+    buffers, idx, mask and threshold keep their bits (and, with a separate
+    `a` buffer, the residual).  After the workspace is zeroed again (and, in
+    place, the residual restored) the same step matches the oracle."""
+    wl = workload.custom(W=4, sizes=[20000, 3000], chunk=256, keep_percent=10,
+                         config_id=530, steps=3)
+    run = GpuRun(wl, "pipeline", inplace=inplace)
+    st = oracle.State(workload.initial_weights(wl))
+    g_np = [workload.all_grads(wl, s) for s in range(2)]
+    g0, g1 = dev_grads(g_np[0]), dev_grads(g_np[1])
+    assert fc.fc_step_path(g0, wl.chunk) == fc.FC_STEP_ONE_LAUNCH
+    run.step(g0)
+    before = run.snapshot()
+    oracle_step(g_np[0], st, wl, before, check_a=False)
+    assert fc.fc_step_status(run.ws, run.N, wl.chunk) == fc.FC_OK
+    fc.fc_test_barrier_loss(5, 20_000_000)
+    run.step(g1)                                   # this one gives up
+    snap = run.snapshot()
+    assert fc.fc_step_status(run.ws, run.N, wl.chunk) == fc.FC_ERR_TIMEOUT
+    unchanged = ["velocity", "weights", "w16", "packed", "packed16", "idx", "mask", "threshold"]
+    if not inplace:
+        unchanged.append("residual")
+    for key in unchanged:
+        assert bits_equal(snap[key], before[key]), key + " changed by a step that gave up"
+    run.ws.zero_()
+    if inplace:
+        run.residual.copy_(torch.from_numpy(before["residual"]).cuda())
+    run.step(g1)
+    oracle_step(g_np[1], st, wl, run.snapshot(), check_a=False)
+    assert fc.fc_step_status(run.ws, run.N, wl.chunk) == fc.FC_OK
+    with pytest.raises(fc.FcError):
+        fc.fc_test_barrier_loss(0, 0)
