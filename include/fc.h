@@ -60,7 +60,9 @@
  *  - Aliasing: only the pairs stated per call may alias.
  *  - Inputs are assumed finite (no inf/NaN in the gradients).
  *  - On error nothing is launched and fc_last_error() describes the cause.
- *  - No kernel waits on another block or on the host, so no call can hang.
+ *  - No kernel waits on the host.  Only the cooperative one-launch step's
+ *    CTAs wait on one another (all resident by the cooperative launch), and
+ *    every wait on the device is bounded (2 s), so no call can hang.
  */
 #ifndef FC_H_
 #define FC_H_
