@@ -1,33 +1,33 @@
 // fc_step in one launch for small problems (a few hundred thousand
-// elements): one thread-block cluster runs a2..a5 with hardware cluster
-// barriers between the phases, instead of three kernels.
+// elements), instead of three kernels.  The three-kernel pipeline pays
+// three launches and two full-device hand-offs per step, which bounds a
+// 133K-element step at 17 us whatever the kernels do.
 //
-// The three-kernel pipeline pays three launches and two full-device
-// hand-offs per step, which bounds a 133K-element step at 17 us whatever
-// the kernels do.  Here the CTAs of one cluster (16 where the GPU allows,
-// else 8) share the work:
-//  1. reduce: warp gw of the cluster takes the 256-element units gw,
-//     gw + nw, ... (nw warps in all) with the tree, unscale and residual of
-//     the register kernel (`k_reduce`), writes `a` and the unit sums of
-//     squares;
-//  2. norms: warp gw finishes the norms of chunks gw, gw + nw, ... from the
-//     unit sums in the fixed float-float order of the selection kernel, and
-//     writes each norm's bit pattern into the shared memory of every CTA of
-//     the cluster (distributed shared memory);
+// Two kernels share the same per-unit code (below) and so give the same
+// bits as the three kernels (the GPU tests compare all of them and the
+// oracle):
+//  * k_step_grid: one cooperative launch, one CTA per SM, with one grid
+//    barrier in the workspace after the norms and the k-th chunk handed to
+//    every CTA through one tag word (both waits bounded);
+//  * k_step_small: one thread-block cluster (16 CTAs where the GPU allows,
+//    else 8) with hardware cluster barriers and distributed shared memory,
+//    for devices that run no cooperative launch.
+// Both run the same four steps:
+//  1. reduce: each warp takes 256-element units with the tree, unscale and
+//     residual of the register kernel (`k_reduce`), and writes `a` and the
+//     unit sums of squares;
+//  2. norms: chunk norms from the unit sums in the fixed float-float order
+//     of the selection kernel (at once, by the reducing warp, when a chunk
+//     is a single unit);
 //  3. select: every chunk's rank in (norm descending, index ascending)
 //     order is counted against all C keys, which each CTA holds; the chunk
-//     of rank k-1 gives the threshold tau and its index c_tau, sent to
-//     every CTA.  Chunk c is kept iff key_c > tau, or key_c == tau and
-//     c <= c_tau: exactly the k chunks first in that order, the same set the
-//     radix select of the pipeline finds;
-//  4. update: warp gw updates its own units again (re-reading the `a` it
+//     of rank k-1 gives the threshold tau and its index c_tau to every CTA.
+//     Chunk c is kept iff key_c > tau, or key_c == tau and c <= c_tau:
+//     exactly the k chunks first in that order, the same set the radix
+//     select of the pipeline finds;
+//  4. update: each warp updates its own units again (re-reading the `a` it
 //     wrote), with each kept chunk's send-buffer slot counted from the keys
 //     (kept chunks before it), exactly as the update kernel does.
-// Every sum and product is the same binary32 operation in the same order
-// as in the three kernels, so the results are the same bits (the GPU tests
-// compare both paths and the oracle).  The cluster barriers are hardware
-// barriers (barrier.cluster with release/acquire at cluster scope): no CTA
-// spins, and no CTA ever waits for anything outside its cluster.
 #include <atomic>
 #include <mutex>
 
