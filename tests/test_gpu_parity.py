@@ -32,15 +32,23 @@ def _compare_paths(p, s):
 
 
 def _run_workload(wl, steps=None, both_paths=True, expect_kernel=None, to_dev=dev_grads):
+    """Steps the pipeline (fc_step) and, with both_paths, the five separate
+    calls; when fc_step runs the layout as one launch, also the three phase
+    calls, so that the phase-1 kernel `expect_kernel` names really runs.
+    Every path must give the same bits, and the oracle's."""
     steps = wl.steps if steps is None else steps
-    runs = [GpuRun(wl, "pipeline")]
-    if both_paths:
-        runs.append(GpuRun(wl, "separate"))
+    runs = None
     st = oracle.State(workload.initial_weights(wl))
     reports = []
     for s in range(steps):
         g_np = workload.all_grads(wl, s)
         g_dev = to_dev(g_np)
+        if runs is None:
+            runs = [GpuRun(wl, "pipeline")]
+            if fc.fc_step_path(g_dev, wl.chunk) != fc.FC_STEP_THREE_KERNELS:
+                runs.append(GpuRun(wl, "phases"))
+            if both_paths:
+                runs.append(GpuRun(wl, "separate"))
         if expect_kernel is not None:
             assert fc.fc_step_reduce_kernel(g_dev, wl.chunk) == expect_kernel
         snaps = []
@@ -48,9 +56,10 @@ def _run_workload(wl, steps=None, both_paths=True, expect_kernel=None, to_dev=de
             r.step(g_dev)
             snaps.append(r.snapshot())
         del g_dev
+        for other in snaps[1:]:
+            _compare_paths(snaps[0], other)
         if both_paths:
-            _compare_paths(snaps[0], snaps[1])
-            assert runs[1].offsets == list(oracle.layout(wl.sizes)[0])
+            assert runs[-1].offsets == list(oracle.layout(wl.sizes)[0])
         reports.append(oracle_step(g_np, st, wl, snaps[-1]))
         del g_np, snaps
     torch.cuda.empty_cache()
@@ -254,11 +263,12 @@ def test_keep_one_and_partial_last_chunk_padding():
     oracle_step(g, oracle.State(workload.initial_weights(wl)), wl, snap)
 
 
-def test_inplace_matches_out_of_place_and_is_deterministic():
+@pytest.mark.parametrize("path", ["pipeline", "phases"])
+def test_inplace_matches_out_of_place_and_is_deterministic(path):
     wl = workload.custom(W=16, sizes=[40000, 123, 70001], chunk=4096, keep_percent=25,
                          config_id=154, steps=3)
-    runs = [GpuRun(wl, "pipeline", inplace=True), GpuRun(wl, "pipeline", inplace=False),
-            GpuRun(wl, "pipeline", inplace=True)]
+    runs = [GpuRun(wl, path, inplace=True), GpuRun(wl, path, inplace=False),
+            GpuRun(wl, path, inplace=True)]
     for s in range(3):
         g = dev_grads(workload.all_grads(wl, s))
         snaps = []
@@ -271,20 +281,21 @@ def test_inplace_matches_out_of_place_and_is_deterministic():
                 assert bits_equal(np.asarray(snaps[0][key]), np.asarray(other[key])), key
 
 
-def test_checkpoint_resume_is_bit_exact():
+@pytest.mark.parametrize("path", ["pipeline", "phases"])
+def test_checkpoint_resume_is_bit_exact(path):
     wl = workload.custom(W=8, sizes=[30000, 5000], chunk=1024, keep_percent=20,
                          config_id=155, steps=5)
     grads = [dev_grads(workload.all_grads(wl, s)) for s in range(5)]
-    straight = GpuRun(wl, "pipeline", inplace=True)
+    straight = GpuRun(wl, path, inplace=True)
     for s in range(5):
         straight.step(grads[s])
     end = straight.snapshot()
-    first = GpuRun(wl, "pipeline", inplace=True)
+    first = GpuRun(wl, path, inplace=True)
     for s in range(3):
         first.step(grads[s])
     torch.cuda.synchronize()
     saved = {k: getattr(first, k).cpu().clone() for k in ("residual", "velocity", "weights")}
-    resumed = GpuRun(wl, "pipeline", inplace=True)
+    resumed = GpuRun(wl, path, inplace=True)
     for k, v in saved.items():
         getattr(resumed, k).copy_(v.cuda())
     for s in range(3, 5):
@@ -294,12 +305,13 @@ def test_checkpoint_resume_is_bit_exact():
         assert bits_equal(end[key], got[key]), key
 
 
-def test_cuda_graph_replay_matches_eager():
+@pytest.mark.parametrize("path", ["pipeline", "phases"])
+def test_cuda_graph_replay_matches_eager(path):
     wl = workload.custom(W=4, sizes=[5000, 77], chunk=256, keep_percent=10,
                          config_id=156, steps=3)
     grads = dev_grads(workload.all_grads(wl, 0))
-    eager = GpuRun(wl, "pipeline", inplace=True)
-    graphed = GpuRun(wl, "pipeline", inplace=True)
+    eager = GpuRun(wl, path, inplace=True)
+    graphed = GpuRun(wl, path, inplace=True)
     table = fc.PtrTable(grads)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -527,8 +539,9 @@ def test_bucketed_gradients_merge_into_one_segment():
     wl = workload.custom(W=16, sizes=[1001, 33, 4099, 7, 60000, 3, 8185],
                          chunk=4096, keep_percent=25, config_id=230, steps=2)
     assert wl.N % 8 == 0
-    sep = GpuRun(wl, "pipeline")
-    buck = GpuRun(wl, "pipeline")
+    sep = GpuRun(wl, "phases")      # phase 1 as its own call: the staged kernel runs
+    buck = GpuRun(wl, "phases")
+    buck1 = GpuRun(wl, "pipeline")  # and the whole step in one launch
     st = oracle.State(workload.initial_weights(wl))
     for s in range(2):
         g_np = workload.all_grads(wl, s)
@@ -542,10 +555,14 @@ def test_bucketed_gradients_merge_into_one_segment():
                 row.append(v)
                 pos += g.size
             views.append(row)
+        if s == 0:
+            assert fc.fc_step_reduce_kernel(views, wl.chunk) == fc.FC_REDUCE_STAGED
         sep.step(dev_grads(g_np))
         buck.step(views)
+        buck1.step(views)
         a, b = sep.snapshot(), buck.snapshot()
         _compare_paths(a, b)
+        _compare_paths(a, buck1.snapshot())
         oracle_step(g_np, st, wl, b)
 
 
@@ -733,13 +750,17 @@ def test_fuzzed_layouts_match_the_oracle(i):
 
     kinds = set()
     run = GpuRun(wl, "pipeline")
+    phases = GpuRun(wl, "phases")   # the phase-1 kernel runs even where fc_step takes one launch
     st = oracle.State(workload.initial_weights(wl))
     for s in range(2):
         g_np = workload.all_grads(wl, s)
         g_dev = to_dev(g_np)
         kinds.add(fc.fc_step_reduce_kernel(g_dev, wl.chunk))
         run.step(g_dev)
-        oracle_step(g_np, st, wl, run.snapshot())
+        phases.step(g_dev)
+        snap = run.snapshot()
+        _compare_paths(snap, phases.snapshot())
+        oracle_step(g_np, st, wl, snap)
     assert len(kinds) == 1
 
 
@@ -779,7 +800,7 @@ def _guard(run):
     dict(W=5, sizes=[1001, 64, 3333], chunk=300, keep_percent=20),            # register
     dict(W=3, sizes=[1234, 7], chunk=100, keep_percent=50),                   # N % 8 != 0
 ], ids=["aligned", "shifted", "register", "ragged"])
-@pytest.mark.parametrize("path", ["pipeline", "separate"])
+@pytest.mark.parametrize("path", ["pipeline", "phases", "separate"])
 def test_no_call_writes_outside_its_buffers(case, path):
     """Guard margins around every output, state and workspace buffer stay
     bit-for-bit untouched over two steps: a memory checker's out-of-bounds
@@ -799,17 +820,26 @@ def test_no_call_writes_outside_its_buffers(case, path):
 
 
 def test_engines_on_several_host_threads_match_sequential_runs():
-    """Four host threads, each stepping its own engine on its own stream
-    (staged shifted, staged aligned, register and large-table layouts), give
+    """Six host threads, each stepping its own engine on its own stream, give
     the bits of the same steps run one after another: the host-side caches
-    and the thread-local tables are safe to use concurrently."""
+    and the thread-local tables are safe to use concurrently.  Four layouts
+    are past the one-launch size (staged shifted, staged aligned, register
+    and large-table), and two run as one cooperative launch each, so those
+    launches from several streams also queue behind one another correctly,
+    each with its own barrier words."""
     import threading
-    cases = [dict(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512, keep_percent=30),
-             dict(W=8, sizes=[4096, 808, 8, 6000], chunk=256, keep_percent=25),
-             dict(W=5, sizes=[1001, 64, 3333], chunk=300, keep_percent=20),
-             dict(W=16, sizes=[97 + 8 * i for i in range(40)], chunk=256, keep_percent=10)]
+    big = 1 << 19
+    cases = [dict(W=16, sizes=[big + 75001, 64, 3333, 2, 700, 5004], chunk=512, keep_percent=30),
+             dict(W=8, sizes=[big, 808, 8, 6000], chunk=256, keep_percent=25),
+             dict(W=5, sizes=[big + 75000, 64, 3333], chunk=300, keep_percent=20),
+             dict(W=16, sizes=[13000 + 8 * i for i in range(40)], chunk=256, keep_percent=10),
+             dict(W=4, sizes=[20000, 3000], chunk=256, keep_percent=10),
+             dict(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512, keep_percent=30)]
+    paths = [fc.FC_STEP_THREE_KERNELS] * 4 + [fc.FC_STEP_ONE_LAUNCH] * 2
     wls = [workload.custom(config_id=420 + i, steps=3, **c) for i, c in enumerate(cases)]
     grads = [[dev_grads(workload.all_grads(wl, s)) for s in range(3)] for wl in wls]
+    for wl, g, path in zip(wls, grads, paths):
+        assert fc.fc_step_path(g[0], wl.chunk) == path
 
     def run(i, engine, stream):
         with torch.cuda.stream(stream):
