@@ -54,10 +54,13 @@ def _write_input(path, wl, steps):
 
 @pytest.mark.gpu
 @pytest.mark.parametrize("case", [
-    None,                                                            # tiny
+    None,                                                            # tiny: one launch
     dict(W=5, sizes=[1001, 64, 3333], chunk=300, keep_percent=20),   # register kernel
-    dict(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512, keep_percent=30),
-], ids=["tiny", "w5", "w16"])
+    dict(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512, keep_percent=30),  # one launch
+    dict(W=16, sizes=[(1 << 19) + 75001, 64, 3333, 2, 700, 5004], chunk=512,
+         keep_percent=30),                                          # shifted staged
+    dict(W=8, sizes=[1 << 19, 808, 8, 6000], chunk=256, keep_percent=25),  # aligned staged
+], ids=["tiny", "w5", "w16", "w16_shifted_staged", "w8_aligned_staged"])
 def test_c_client_matches_the_oracle(fc_lib, tmp_path, case):
     wl = workload.get("tiny") if case is None else workload.custom(config_id=410, steps=2, **case)
     steps = 2
