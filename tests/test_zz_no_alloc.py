@@ -35,16 +35,20 @@ def _noalloc_step(run, grads):
                        run.packed16, run.send_scale)
 
 
-@pytest.mark.parametrize("name", ["tiny", "custom", "shifted"])
+@pytest.mark.parametrize("name", ["tiny", "custom", "shifted", "shifted_big"])
 def test_noalloc_matches_workspace_pipeline_on_two_calls(name):
-    if name == "tiny":
+    if name == "tiny":                # one launch
         wl = workload.get("tiny")
-    elif name == "custom":
+    elif name == "custom":            # one launch (7 workers)
         wl = workload.custom(W=7, sizes=[5000, 33, 12000], chunk=1000, keep_percent=30,
                              config_id=170, steps=2)
-    else:                             # the staged kernel's shifted layout
+    elif name == "shifted":           # one launch
         wl = workload.custom(W=16, sizes=[1001, 64, 3333, 2, 700, 5004], chunk=512,
                              keep_percent=30, config_id=171, steps=2)
+    else:                             # past the one-launch size: the staged kernel's
+        # shifted layout, the selection and the update kernels
+        wl = workload.custom(W=16, sizes=[(1 << 19) + 75001, 64, 3333, 2, 700, 5004],
+                             chunk=512, keep_percent=30, config_id=172, steps=2)
     ref = GpuRun(wl, "pipeline")      # fc_step with a caller workspace
     new = GpuRun(wl, "pipeline")      # same buffers, stepped by fc_step_noalloc
     st = oracle.State(workload.initial_weights(wl))
