@@ -78,8 +78,8 @@ size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
 // reduction's failure word; 2: the last step's outcome, 0 = applied; 4-5:
 // the staged reduction's 64-bit counter of dynamically handed-out tiles; 6:
 // its count of finished producers; all but word 2 zero between calls;
-// 8-12: the one-launch grid step's barrier count and generation and its
-// hand-off of the k-th chunk) and the kept-slot map (int32 [C]).
+// 8-12: the one-launch grid step's 64-bit barrier count and its hand-off
+// of the k-th chunk) and the kept-slot map (int32 [C]).
 struct WsLayout {
     size_t partials, counters, slot, total;
 };

@@ -56,14 +56,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns()
     return t;
 }
 
-__device__ __forceinline__ uint32_t atom_add_acq_rel_gpu(unsigned *p, uint32_t v)
-{
-    uint32_t old;
-    asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v)
-                 : "memory");
-    return old;
-}
-
 __device__ __forceinline__ void st_release_gpu(unsigned *p, uint32_t v)
 {
     asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -84,29 +76,37 @@ __device__ __forceinline__ bool wait_equal_gpu(const unsigned *p, uint32_t v, ui
     return true;
 }
 
-// Barrier over all nblocks CTAs of a cooperative launch (every CTA resident
-// at once), on two words in global memory: bar[0] counts arrivals (zero
-// between barriers), bar[1] is the generation.  Thread 0 of each CTA reads
-// the generation g and arrives with an acquire-release add, which also
-// publishes the CTA's writes (ordered before it by the CTA barrier); the
-// last CTA to arrive clears the count and releases generation g + 1, for
-// which the others wait, at most limit_ns.  Returns false, in every thread
-// of the CTA, if that wait ran out (the caller then gives up the step);
-// *gen_out is g + 1.
-__device__ __forceinline__ bool grid_sync(unsigned *bar, unsigned nblocks, uint64_t limit_ns,
-                                          volatile uint32_t *s_ok, volatile uint32_t *s_gen)
+__device__ __forceinline__ uint64_t ld_acquire_gpu_u64(const unsigned long long *p)
+{
+    uint64_t v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
+// Barrier over all n CTAs of a cooperative launch on a 64-bit arrival count
+// that only grows (zero in a fresh workspace).  Each completed launch adds
+// n per barrier, so between launches the count is a multiple of n, and
+// *s_base, read by thread 0 at launch start and rounded down to a multiple
+// of n, is the count before this launch even if other CTAs have already
+// arrived.  At barrier k (1, 2, ...) thread 0 of each CTA adds one with a
+// release reduction (no return value to wait for) and waits, at most
+// limit_ns, until the count reaches *s_base + k n.  Returns false, in every
+// thread of the CTA, if that wait ran out (a launch that gave up leaves the
+// count off its multiple of n, so the workspace must be zeroed again).
+__device__ __forceinline__ bool grid_arrive_wait(unsigned long long *count, const uint64_t *s_base,
+                                                 unsigned k, uint64_t limit_ns,
+                                                 volatile uint32_t *s_ok)
 {
     __syncthreads();
     if (threadIdx.x == 0) {
-        const unsigned g = ld_acquire_gpu(bar + 1);
-        bool ok = true;
-        if (atom_add_acq_rel_gpu(bar, 1u) == nblocks - 1) {
-            st_relaxed_gpu(bar, 0u);
-            st_release_gpu(bar + 1, g + 1u);
-        } else {
-            ok = wait_equal_gpu(bar + 1, g + 1u, limit_ns);
+        const uint64_t target = *s_base + (uint64_t)k * gridDim.x;
+        asm volatile("red.release.gpu.global.add.u64 [%0], 1;" ::"l"(count) : "memory");
+        bool ok = ld_acquire_gpu_u64(count) >= target;
+        if (!ok) {
+            const uint64_t t0 = globaltimer_ns();
+            while (!(ok = ld_acquire_gpu_u64(count) >= target))
+                if (globaltimer_ns() - t0 > limit_ns) break;
         }
-        *s_gen = g + 1u;
         *s_ok = ok ? 1u : 0u;
     }
     __syncthreads();

@@ -97,9 +97,9 @@ struct SmallStep {
     float *packed;
     __half *packed16;
     float send_scale;
-    unsigned *bar;           // five workspace words for the grid kernel (barrier
-                             // count, generation, the k-th chunk and its tag);
-                             // NULL: cluster kernel only
+    unsigned *bar;           // five workspace words for the grid kernel (64-bit
+                             // barrier count, the k-th chunk and its tag),
+                             // 8-byte aligned; NULL: cluster kernel only
 };
 
 // Launches the whole step as one kernel when the problem and the device

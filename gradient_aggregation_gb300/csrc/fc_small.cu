@@ -7,8 +7,8 @@
 // bits as the three kernels (the GPU tests compare all of them and the
 // oracle):
 //  * k_step_grid: one cooperative launch, one CTA per SM, with one grid
-//    barrier in the workspace after the norms and the k-th chunk handed to
-//    every CTA through one tag word (both waits bounded);
+//    barrier on a workspace arrival count after the norms and the k-th
+//    chunk handed to every CTA through one tag word (both waits bounded);
 //  * k_step_small: one thread-block cluster (16 CTAs where the GPU allows,
 //    else 8) with hardware cluster barriers and distributed shared memory,
 //    for devices that run no cooperative launch.
@@ -55,7 +55,7 @@ struct SmallArgs {
     __half *packed16;
     float send_scale;
     int inplace;
-    unsigned *bar;      // grid kernel: barrier count, generation, tau, c_tau, tau's tag
+    unsigned *bar;      // grid kernel: 64-bit arrival count (words 0-1), tau, c_tau, tau's tag
     uint64_t limit_ns;  // grid kernel: longest wait at a barrier
     int drop_cta;       // grid kernel, test hook: this CTA skips its first barrier (-1: none)
 };
@@ -383,11 +383,11 @@ __global__ void __launch_bounds__(NT, 1)
 // ---- the grid kernel ------------------------------------------------------------
 //
 // The same step over every SM: one cooperative launch (all CTAs resident at
-// once) with a grid barrier in global memory after the norms (two when a
-// chunk has several units).  The warp that finds the chunk of rank k-1 then
-// publishes it (tau, c_tau) with a release store of the barrier's
-// generation, and every CTA waits for that word alone instead of a second
-// barrier.  Units and chunks are dealt to warps across the CTAs (warp index
+// once) with a grid barrier after the norms (two when a chunk has several
+// units) on an arrival count in the workspace (grid_arrive_wait).  The warp
+// that finds the chunk of rank k-1 then publishes it (tau, c_tau) with a
+// release store of a tag, the count this launch's last barrier waited for,
+// and every CTA waits for that word alone instead of a second barrier.  Units and chunks are dealt to warps across the CTAs (warp index
 // gw = warp * CTAs + CTA), so a small problem's units spread over all SMs.
 // A barrier wait that runs out (only possible if the GPU stalls for
 // limit_ns) ends every CTA that sees it without writing v, w or the
@@ -399,7 +399,8 @@ __global__ void __launch_bounds__(NT, 1)
     constexpr int kWarps = NT / 32;
     __shared__ __align__(16) uint32_t skeys[FC_SMALL_MAX_CHUNKS + 4];
     __shared__ uint32_t s_kept[FC_SMALL_MAX_CHUNKS / 32], s_before[FC_SMALL_MAX_CHUNKS / 32];
-    __shared__ uint32_t s_ok, s_gen, s_tau, s_ctau;
+    __shared__ uint32_t s_ok, s_tau, s_ctau;
+    __shared__ uint64_t s_base;
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int64_t gw = (int64_t)warp * gridDim.x + blockIdx.x;
     const int64_t nw = (int64_t)gridDim.x * kWarps;
@@ -410,8 +411,14 @@ __global__ void __launch_bounds__(NT, 1)
     };
     // Launched after whatever the stream ran before (programmatic
     // serialisation): no global memory is touched before that work is done.
+    unsigned long long *count = reinterpret_cast<unsigned long long *>(A.bar);
     wait_for_prior_grid();
     allow_dependent_launch();
+    // the barrier's arrival count before this launch (see grid_arrive_wait)
+    if (threadIdx.x == 0) {
+        const uint64_t c = ld_acquire_gpu_u64(count);
+        s_base = c - c % gridDim.x;
+    }
 
     // ---- 1. reduce (and, with one unit per chunk, the chunk's norm)
     for (int64_t un = gw; un < G.units; un += nw) {
@@ -428,12 +435,14 @@ __global__ void __launch_bounds__(NT, 1)
     // test hook: this CTA never arrives, so the others' waits run out
     if ((int)blockIdx.x == A.drop_cta) return give_up();
     // ---- 2. norms of chunks of several units
+    unsigned barriers = 1;
     if (G.U > 1) {
-        if (!grid_sync(A.bar, gridDim.x, A.limit_ns, &s_ok, &s_gen)) return give_up();
+        if (!grid_arrive_wait(count, &s_base, barriers++, A.limit_ns, &s_ok)) return give_up();
         chunk_norms_from_units(A, gw, nw, lane, [](int64_t, uint32_t) {});
     }
-    if (!grid_sync(A.bar, gridDim.x, A.limit_ns, &s_ok, &s_gen)) return give_up();
-    const uint32_t tag = s_gen;
+    if (!grid_arrive_wait(count, &s_base, barriers, A.limit_ns, &s_ok)) return give_up();
+    // this launch's last barrier count: differs from every earlier launch's
+    const uint32_t tag = (uint32_t)(s_base + (uint64_t)barriers * gridDim.x);
 
     // every CTA takes all keys
     for (int64_t c = threadIdx.x; c < C; c += NT) skeys[c] = __float_as_uint(__ldcg(A.norms + c));
