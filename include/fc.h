@@ -363,9 +363,9 @@ FC_API fc_status fc_step_update(const float *a, int64_t N, int64_t chunk,
  *                  residual before running the step again.  The same status
  *                  comes from a one-launch step (FC_STEP_ONE_LAUNCH) whose
  *                  grid barrier wait ran out: nothing but `a`, the norms and
- *                  the unit sums was written, and the barrier's words are
- *                  left mid-way, so zero the workspace again (as before its
- *                  first use) before the next step.
+ *                  the unit sums was written, and the barrier's arrival
+ *                  count is left part-way, so zero the workspace again (as
+ *                  before its first use) before the next step.
  * Other statuses: bad arguments or a failed CUDA call. */
 FC_API fc_status fc_step_status(const void *workspace, size_t workspace_bytes,
                                 int64_t N, int64_t chunk, void *stream);
