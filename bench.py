@@ -399,7 +399,7 @@ def step_algorithmic_bytes(wl, k: int) -> dict:
     phase2 = 4 * units + 4 * C + C + 4 * C + 4 * k
     phase3 = 16 * N + 8 * kept_el + 4 * k * wl.chunk   # + the zero-padded send slots
     return {"phase1": phase1, "phase2": phase2, "phase3": phase3,
-            "step": phase1 + phase2 + phase3, "survey": N * (2 * W + 32)}
+            "step": phase1 + phase2 + phase3, "full_count": N * (2 * W + 32)}
 
 
 def max_over_ranks(x: float, device=None) -> float:
@@ -870,10 +870,10 @@ def run_gpu(args, wl, rank, world, local):
                          "timed_launches": len(reduce_ms),
                          "isolated": iso},
             "step_roofline": {"algorithmic_bytes_per_step": int(step_alg),
-                              "survey_count_bytes_per_step": int(alg["survey"]),
+                              "full_count_bytes_per_step": int(alg["full_count"]),
                               "achieved_gbs": round(step_alg / (ms_per_step / 1e3) / 1e9, 1),
                               "frac": round(step_alg / (ms_per_step / 1e3) / 1e9 / peak, 4),
-                              "survey_count_frac": round(alg["survey"] / (ms_per_step / 1e3)
+                              "full_count_frac": round(alg["full_count"] / (ms_per_step / 1e3)
                                                          / 1e9 / peak, 4),
                               "select_update_ms": round(rest_ms, 5)},
             "cpu_baseline": cpu,

@@ -28,7 +28,7 @@ def dev_grads(grads_np, device="cuda"):
     return [[torch.from_numpy(g).to(device) for g in row] for row in grads_np]
 
 
-class GpuRun:
+class DeviceRun:
     """Device state and buffers of one engine instance for a workload."""
 
     def __init__(self, wl: workload.Workload, path: str = "pipeline",

@@ -146,7 +146,7 @@ def test_algorithmic_bytes_per_kernel():
     b = bench.step_algorithmic_bytes(wl, 20)
     assert b["phase1"] == 2 * W * N + 8 * N + 4 * units == 2_496_108_424
     assert b["phase3"] == 16 * N + 8 * 20 * 32768 + 4 * 20 * 32768
-    assert b["survey"] == N * (2 * W + 32)
+    assert b["full_count"] == N * (2 * W + 32)
     assert b["step"] == b["phase1"] + b["phase2"] + b["phase3"]
     # keep-all: every element's a read, residual zeroed, send slots for all chunks
     nin = workload.get("nin")

@@ -13,7 +13,7 @@ import torch
 
 import oracle
 from gradient_aggregation_gb300 import fc, workload
-from tests.gpu_util import GpuRun, bits_equal, dev_grads, oracle_step
+from tests.gpu_util import DeviceRun, bits_equal, dev_grads, oracle_step
 
 pytestmark = pytest.mark.gpu
 
@@ -44,11 +44,11 @@ def _run_workload(wl, steps=None, both_paths=True, expect_kernel=None, to_dev=de
         g_np = workload.all_grads(wl, s)
         g_dev = to_dev(g_np)
         if runs is None:
-            runs = [GpuRun(wl, "pipeline")]
+            runs = [DeviceRun(wl, "pipeline")]
             if fc.fc_step_path(g_dev, wl.chunk) != fc.FC_STEP_THREE_KERNELS:
-                runs.append(GpuRun(wl, "phases"))
+                runs.append(DeviceRun(wl, "phases"))
             if both_paths:
-                runs.append(GpuRun(wl, "separate"))
+                runs.append(DeviceRun(wl, "separate"))
         if expect_kernel is not None:
             assert fc.fc_step_reduce_kernel(g_dev, wl.chunk) == expect_kernel
         snaps = []
@@ -184,8 +184,8 @@ def test_misaligned_gradient_pointers():
     wl = workload.custom(W=6, sizes=[1001, 64, 3333], chunk=300, keep_percent=20,
                          config_id=150, steps=2)
     st = oracle.State(workload.initial_weights(wl))
-    run = GpuRun(wl, "pipeline")
-    sep = GpuRun(wl, "separate")
+    run = DeviceRun(wl, "pipeline")
+    sep = DeviceRun(wl, "separate")
     for s in range(2):
         g_np = workload.all_grads(wl, s)
         g_dev = []
@@ -210,7 +210,7 @@ def test_fused_buffer_with_ragged_rows():
     wl = workload.custom(W=3, sizes=[1234, 7], chunk=100, keep_percent=50,
                          config_id=151, steps=1)
     g_np = workload.all_grads(wl, 0)
-    run = GpuRun(wl, "separate")
+    run = DeviceRun(wl, "separate")
     run.step(dev_grads(g_np))
     oracle_step(g_np, oracle.State(workload.initial_weights(wl)), wl, run.snapshot())
 
@@ -222,7 +222,7 @@ def test_ties_keep_lowest_indices():
     wl = workload.custom(W=W, sizes=[N], chunk=cs, keep_percent=30, config_id=152)
     g = [[np.full(N, 2.0, dtype=np.float16)] for _ in range(W)]
     for path in ("pipeline", "phases", "separate"):
-        run = GpuRun(wl, path)
+        run = DeviceRun(wl, path)
         run.step(dev_grads(g))
         snap = run.snapshot()
         assert list(snap["idx"]) == [0, 1, 2]
@@ -243,7 +243,7 @@ def test_threshold_inside_a_group_of_ties(C):
     rest = [c for c in range(C) if c % 5][: k - len(big)]
     want = sorted(big + rest)
     for path in ("pipeline", "phases", "separate"):
-        run = GpuRun(wl, path)
+        run = DeviceRun(wl, path)
         run.step(dev_grads(g))
         snap = run.snapshot()
         assert list(snap["idx"]) == want, path
@@ -254,7 +254,7 @@ def test_keep_one_and_partial_last_chunk_padding():
     wl = workload.custom(W=2, sizes=[1000], chunk=300, keep_percent=1, config_id=153)
     g = [[np.zeros(1000, np.float16)] for _ in range(2)]
     g[0][0][950:] = 4.0       # the short last chunk (100 elements) wins
-    run = GpuRun(wl, "pipeline")
+    run = DeviceRun(wl, "pipeline")
     run.packed.fill_(7.0)
     run.step(dev_grads(g))
     snap = run.snapshot()
@@ -267,8 +267,8 @@ def test_keep_one_and_partial_last_chunk_padding():
 def test_inplace_matches_out_of_place_and_is_deterministic(path):
     wl = workload.custom(W=16, sizes=[40000, 123, 70001], chunk=4096, keep_percent=25,
                          config_id=154, steps=3)
-    runs = [GpuRun(wl, path, inplace=True), GpuRun(wl, path, inplace=False),
-            GpuRun(wl, path, inplace=True)]
+    runs = [DeviceRun(wl, path, inplace=True), DeviceRun(wl, path, inplace=False),
+            DeviceRun(wl, path, inplace=True)]
     for s in range(3):
         g = dev_grads(workload.all_grads(wl, s))
         snaps = []
@@ -286,16 +286,16 @@ def test_checkpoint_resume_is_bit_exact(path):
     wl = workload.custom(W=8, sizes=[30000, 5000], chunk=1024, keep_percent=20,
                          config_id=155, steps=5)
     grads = [dev_grads(workload.all_grads(wl, s)) for s in range(5)]
-    straight = GpuRun(wl, path, inplace=True)
+    straight = DeviceRun(wl, path, inplace=True)
     for s in range(5):
         straight.step(grads[s])
     end = straight.snapshot()
-    first = GpuRun(wl, path, inplace=True)
+    first = DeviceRun(wl, path, inplace=True)
     for s in range(3):
         first.step(grads[s])
     torch.cuda.synchronize()
     saved = {k: getattr(first, k).cpu().clone() for k in ("residual", "velocity", "weights")}
-    resumed = GpuRun(wl, path, inplace=True)
+    resumed = DeviceRun(wl, path, inplace=True)
     for k, v in saved.items():
         getattr(resumed, k).copy_(v.cuda())
     for s in range(3, 5):
@@ -310,8 +310,8 @@ def test_cuda_graph_replay_matches_eager(path):
     wl = workload.custom(W=4, sizes=[5000, 77], chunk=256, keep_percent=10,
                          config_id=156, steps=3)
     grads = dev_grads(workload.all_grads(wl, 0))
-    eager = GpuRun(wl, path, inplace=True)
-    graphed = GpuRun(wl, path, inplace=True)
+    eager = DeviceRun(wl, path, inplace=True)
+    graphed = DeviceRun(wl, path, inplace=True)
     table = fc.PtrTable(grads)
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
@@ -337,7 +337,7 @@ def test_device_argument_errors():
         fc.fc_chunk_norms(a[1:], 999, 10, torch.empty(100, device=dev))
     assert e.value.status == fc.FC_ERR_ALIGNMENT
     wl = workload.custom(W=2, sizes=[1000], chunk=100, keep_percent=10, config_id=157)
-    run = GpuRun(wl, "pipeline")
+    run = DeviceRun(wl, "pipeline")
     run.ws = run.ws[:16]
     with pytest.raises(fc.FcError) as e:
         run.step(dev_grads(workload.all_grads(wl, 0)))
@@ -499,7 +499,7 @@ def test_staged_reduction_reports_a_wait_that_runs_out(sizes, kind, inplace):
     matches the oracle.  The context stays usable throughout."""
     wl = workload.custom(W=16, sizes=sizes, chunk=4096, keep_percent=25,
                          config_id=220, steps=3)
-    run = GpuRun(wl, "pipeline", inplace=inplace)
+    run = DeviceRun(wl, "pipeline", inplace=inplace)
     st = oracle.State(workload.initial_weights(wl))
     g_np = [workload.all_grads(wl, s) for s in range(2)]
     g0, g1 = dev_grads(g_np[0]), dev_grads(g_np[1])
@@ -539,9 +539,9 @@ def test_bucketed_gradients_merge_into_one_segment():
     wl = workload.custom(W=16, sizes=[1001, 33, 4099, 7, 60000, 3, 8185],
                          chunk=4096, keep_percent=25, config_id=230, steps=2)
     assert wl.N % 8 == 0
-    sep = GpuRun(wl, "phases")      # phase 1 as its own call: the staged kernel runs
-    buck = GpuRun(wl, "phases")
-    buck1 = GpuRun(wl, "pipeline")  # and the whole step in one launch
+    sep = DeviceRun(wl, "phases")      # phase 1 as its own call: the staged kernel runs
+    buck = DeviceRun(wl, "phases")
+    buck1 = DeviceRun(wl, "pipeline")  # and the whole step in one launch
     st = oracle.State(workload.initial_weights(wl))
     for s in range(2):
         g_np = workload.all_grads(wl, s)
@@ -749,8 +749,8 @@ def test_fuzzed_layouts_match_the_oracle(i):
         return out
 
     kinds = set()
-    run = GpuRun(wl, "pipeline")
-    phases = GpuRun(wl, "phases")   # the phase-1 kernel runs even where fc_step takes one launch
+    run = DeviceRun(wl, "pipeline")
+    phases = DeviceRun(wl, "phases")   # the phase-1 kernel runs even where fc_step takes one launch
     st = oracle.State(workload.initial_weights(wl))
     for s in range(2):
         g_np = workload.all_grads(wl, s)
@@ -770,7 +770,7 @@ _GUARD_FILL = {torch.float32: (torch.int32, 0x7FA5A5A5), torch.int32: (torch.int
 
 
 def _guard(run):
-    """Moves every device buffer of a GpuRun into the middle of a larger
+    """Moves every device buffer of a DeviceRun into the middle of a larger
     tensor whose margins (512 bytes each side) hold a sentinel pattern;
     returns the bases and their original contents."""
     saved = []
@@ -806,7 +806,7 @@ def test_no_call_writes_outside_its_buffers(case, path):
     bit-for-bit untouched over two steps: a memory checker's out-of-bounds
     write detection, done by the test itself."""
     wl = workload.custom(config_id=400, steps=2, **case)
-    run = GpuRun(wl, path)
+    run = DeviceRun(wl, path)
     saved = _guard(run)
     st = oracle.State(workload.initial_weights(wl))
     for s in range(2):
@@ -914,8 +914,8 @@ def test_one_launch_step_matches_three_kernels_and_the_oracle(name, inplace, one
     included)."""
     kw = ONE_LAUNCH_CASES[name]
     wl = workload.get(name) if kw is None else workload.custom(config_id=500, steps=2, **kw)
-    one = GpuRun(wl, "pipeline", inplace=inplace)
-    three = GpuRun(wl, "phases", inplace=inplace)
+    one = DeviceRun(wl, "pipeline", inplace=inplace)
+    three = DeviceRun(wl, "phases", inplace=inplace)
     st = oracle.State(workload.initial_weights(wl))
     for s in range(2):
         g_np = workload.all_grads(wl, s)
@@ -935,7 +935,7 @@ def test_one_launch_step_with_ties_and_misaligned_pointers(one_launch_kind):
     wl = workload.custom(W=4, sizes=[2048, 2048], chunk=256, keep_percent=25,
                          config_id=510, steps=1)
     g_np = [[np.full(n, 0.5, np.float16) for n in wl.sizes] for _ in range(wl.W)]
-    one = GpuRun(wl, "pipeline")
+    one = DeviceRun(wl, "pipeline")
     st = oracle.State(workload.initial_weights(wl))
     out = []
     for w, row in enumerate(g_np):
@@ -987,7 +987,7 @@ def test_one_launch_barrier_wait_runs_out(inplace):
     place, the residual restored) the same step matches the oracle."""
     wl = workload.custom(W=4, sizes=[20000, 3000], chunk=256, keep_percent=10,
                          config_id=530, steps=3)
-    run = GpuRun(wl, "pipeline", inplace=inplace)
+    run = DeviceRun(wl, "pipeline", inplace=inplace)
     st = oracle.State(workload.initial_weights(wl))
     g_np = [workload.all_grads(wl, s) for s in range(2)]
     g0, g1 = dev_grads(g_np[0]), dev_grads(g_np[1])

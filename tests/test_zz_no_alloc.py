@@ -16,7 +16,7 @@ import torch
 
 import oracle
 from gradient_aggregation_gb300 import fc, workload
-from tests.gpu_util import GpuRun, bits_equal, dev_grads, assert_close, oracle_step, RTOL_F32
+from tests.gpu_util import DeviceRun, bits_equal, dev_grads, assert_close, oracle_step, RTOL_F32
 
 pytestmark = pytest.mark.gpu
 
@@ -49,8 +49,8 @@ def test_noalloc_matches_workspace_pipeline_on_two_calls(name):
         # shifted layout, the selection and the update kernels
         wl = workload.custom(W=16, sizes=[(1 << 19) + 75001, 64, 3333, 2, 700, 5004],
                              chunk=512, keep_percent=30, config_id=172, steps=2)
-    ref = GpuRun(wl, "pipeline")      # fc_step with a caller workspace
-    new = GpuRun(wl, "pipeline")      # same buffers, stepped by fc_step_noalloc
+    ref = DeviceRun(wl, "pipeline")      # fc_step with a caller workspace
+    new = DeviceRun(wl, "pipeline")      # same buffers, stepped by fc_step_noalloc
     st = oracle.State(workload.initial_weights(wl))
     for step in range(2):
         g_np = workload.all_grads(wl, step)
@@ -74,7 +74,7 @@ def test_noalloc_keeps_the_callers_current_device():
     wl = workload.get("tiny")
     dev = 1 if torch.cuda.device_count() > 1 else 0
     torch.cuda.set_device(0)
-    run = GpuRun(wl, "pipeline", device="cuda:%d" % dev)
+    run = DeviceRun(wl, "pipeline", device="cuda:%d" % dev)
     g = dev_grads(workload.all_grads(wl, 0), device="cuda:%d" % dev)
     with torch.cuda.device(dev):
         stream = torch.cuda.current_stream().cuda_stream
