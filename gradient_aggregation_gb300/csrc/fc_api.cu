@@ -665,7 +665,14 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
             fill_table(tab, grads, W, L, sizes);
             e = launch_step_small(tab, st, (cudaStream_t)stream, false, &launched);
         }
-        if (e != cudaSuccess) return cuda_fail(e, "step_small launch");
+        if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidClusterSize) {
+            // the device cannot hold the launch right now (another context
+            // holds SMs, or a partitioned GPU): the three kernels instead
+            (void)cudaGetLastError();
+            launched = FC_STEP_THREE_KERNELS;
+        } else if (e != cudaSuccess) {
+            return cuda_fail(e, "step_small launch");
+        }
         if (launched != FC_STEP_THREE_KERNELS) return ok();
     }
     TRY(fc_step_reduce(grads, W, L, sizes, loss_scale, chunk, residual, a,
