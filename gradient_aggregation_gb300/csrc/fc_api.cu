@@ -666,8 +666,9 @@ fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
             e = launch_step_small(tab, st, (cudaStream_t)stream, false, &launched);
         }
         if (e == cudaErrorCooperativeLaunchTooLarge || e == cudaErrorInvalidClusterSize) {
-            // the device cannot hold the launch right now (another context
-            // holds SMs, or a partitioned GPU): the three kernels instead
+            // the device cannot hold the launch at all (for instance a
+            // context limited to a share of the SMs): the three kernels
+            // instead
             (void)cudaGetLastError();
             launched = FC_STEP_THREE_KERNELS;
         } else if (e != cudaSuccess) {

@@ -373,9 +373,9 @@ FC_API fc_status fc_step_status(const void *workspace, size_t workspace_bytes,
 /* Phases 1-3 in one call on one stream.  Small problems run as one launch
  * (see fc_step_path); all others as the three kernels of fc_step_reduce,
  * fc_step_select and fc_step_update.  All give the same bits.  If the
- * device refuses the one launch for lack of room (a cooperative launch
- * that does not fit while other work holds SMs), the call takes the three
- * kernels instead. */
+ * device refuses the one launch as too large for it (for instance a context
+ * limited to a share of the SMs), the call takes the three kernels
+ * instead. */
 FC_API fc_status fc_step(const void *const *grads, int32_t W, int32_t L,
                          const int64_t *sizes, float loss_scale, int64_t chunk,
                          int64_t k, float lr, float momentum, float *residual,
