@@ -1,9 +1,9 @@
 // Phase 1 (a2 + unit sums of squares) with TMA staging, for 4, 8 or 16
 // workers, N a multiple of 8 and a chunk size that is a multiple of 256.
 //
-// One CTA per SM: a producer warp streams tiles of TT fused elements of all
-// W workers (and the residual) from HBM into a ring of S shared-memory stages
-// with bulk copies (cp.async.bulk, completion counted on an mbarrier); eight
+// One CTA per SM (two with worker halves, below): a producer warp streams
+// tiles of TT fused elements of all W workers (and the residual) from HBM
+// into a ring of S shared-memory stages with bulk copies (cp.async.bulk, completion counted on an mbarrier); eight
 // consumer warps take one 256-element unit each per tile, add the workers in
 // the same binary tree as the register kernel (k_reduce) from shared memory,
 // and write `a` and the unit sums of squares exactly as k_reduce does, so the
@@ -30,6 +30,18 @@
 //    (FC_TMA_SHIFTED_MIN_TILES) also take this variant, with every shift 0:
 //    it measured faster on long runs.  Aligned mid-size runs go to the
 //    register kernel instead (see tma_layout).
+//
+// Worker halves (shifted layout, 16 workers): each tile goes through the
+// ring as two stages, the first holding workers 0..7 and the second workers
+// 8..15, with two CTAs per SM (each about 100 KB of stages, residual read
+// by the consumers from global memory).  A consumer warp keeps the first
+// half's subtree in registers and adds the second's to it: in the binary
+// tree of 16 leaves those two subtrees are joined last, so the bits do not
+// change.  Two producers and sixteen consumer warps per SM: the GoogLeNet-
+// shaped phase 1 (many short layers, so many short copies per tile) went
+// from 55.0 to 51.7 us; the AlexNet-shaped one was unchanged (350 us), and
+// with 8 workers the halves gained nothing in phase 1 and lost 3 us in the
+// step, so 8 workers keep one stage per tile.
 //
 // Tile order: CTA b takes tiles b, b + grid, b + 2 grid, ...  In long
 // launches (kDynMinRounds rounds or more) that holds for all but the last
@@ -174,13 +186,14 @@ __device__ __forceinline__ int layer_shift(const Tab &tab, int l)
 // of producers that have finished with it (all zero between launches).
 // drop_tile >= 0 (test hook only, see fc_test_stage_loss): the producer
 // issues no copies for that tile, so the bounded waits on it run out.
-template <class Tab, int WT, int MAXH, bool MIS>
-__global__ void __launch_bounds__(kThreads, 1)
+template <class Tab, int WT, int MAXH, bool MIS, int NH>
+__global__ void __launch_bounds__(kThreads, NH)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
                  float *partials, unsigned *ctr, const int64_t drop_tile,
                  const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end)
 {
+    static_assert(NH == 1 || (MIS && WT == 16), "worker halves: shifted layout, 16 workers");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
     unsigned char *stages = smem + 128;
@@ -188,11 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     unsigned long long *dyn_next = reinterpret_cast<unsigned long long *>(ctr + 4);
     unsigned *dyn_done = ctr + 6;
     const int W = WT > 0 ? WT : tab.W;
+    const int WH = W / NH;  // worker rows per stage
     const int L = tab.L;
     const int ROW = TT + (MIS ? kSlack : 0);  // elements per worker row
-    const size_t gbytes = (size_t)W * ROW * 2;
-    const size_t sbytes =
-        gbytes + (size_t)TT * 4 + (MIS ? kMaxPieces * sizeof(int4) : 0) + kStageHead;
+    const size_t gbytes = (size_t)WH * ROW * 2;
+    // with one stage per tile the residual is staged too; with halves the
+    // consumers read it from global memory
+    const size_t rreg = NH == 1 ? (size_t)TT * 4 : 0;
+    const size_t sbytes = gbytes + rreg + (MIS ? kMaxPieces * sizeof(int4) : 0) + kStageHead;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     // tiles of TT fused elements from f_begin (a multiple of 256) to f_end
     const int64_t ntiles = (f_end - f_begin + TT - 1) / TT;
@@ -216,15 +232,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (warp == kConsumerWarps) {
         // producer
         if (lane != 0) return;
-        // Fills stage s with tile t (its index first, for the consumers).
-        auto issue = [&](int s, int64_t t) {
+        // Fills stage s with worker half h of tile t (its index and half
+        // first, for the consumers).
+        auto issue = [&](int s, int64_t t, int h) {
             const uint32_t full = smem_u32(&bars[s]);
             unsigned char *st = stages + (size_t)s * sbytes;
-            *reinterpret_cast<volatile int64_t *>(st + sbytes - kStageHead) = t;
+            volatile int64_t *head = reinterpret_cast<volatile int64_t *>(st + sbytes - kStageHead);
+            head[0] = t * NH + h;
             if (t == drop_tile) return;
             const int64_t f0 = f_begin + t * TT;
             const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
-            const uint32_t rbytes = resid ? (uint32_t)((f1 - f0) * 4) : 0u;
+            const uint32_t rbytes = NH == 1 && resid ? (uint32_t)((f1 - f0) * 4) : 0u;
+            const int w0 = h * WH;
             if constexpr (!MIS) {
                 mbar_expect_tx(full, (uint32_t)((f1 - f0) * 2 * W) + rbytes);
                 int l = find_layer(tab, f0);
@@ -241,12 +260,24 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // Piece table: {end of the piece (tile-relative), sh (or -1
                 // if unstaged), layer, copied range [lo, hi) of the row as
                 // lo | hi << 16}.  The last entry always ends at the tile's end.
-                int4 *pieces = reinterpret_cast<int4 *>(st + gbytes + (size_t)TT * 4);
+                // The second half of a tile copies the first half's table
+                // (the stage issued just before), with its count and row bytes
+                // from that stage's head.
+                int4 *pieces = reinterpret_cast<int4 *>(st + gbytes + rreg);
                 int n = 0;
-                int64_t prev_phi = 0;  // end of the last staged piece's frames
                 uint32_t row_bytes = 0;
+                if (h > 0) {
+                    const unsigned char *pst = stages + (size_t)((s + S - 1) % S) * sbytes;
+                    const volatile int32_t *ph =
+                        reinterpret_cast<const volatile int32_t *>(pst + sbytes - kStageHead);
+                    n = ph[2];
+                    row_bytes = (uint32_t)ph[3];
+                    const int4 *pp = reinterpret_cast<const int4 *>(pst + gbytes + rreg);
+                    for (int i = 0; i < n; ++i) pieces[i] = pp[i];
+                }
+                int64_t prev_phi = 0;  // end of the last staged piece's frames
                 int l = find_layer(tab, f0);
-                for (int64_t fa = f0; fa < f1;) {
+                for (int64_t fa = f0; fa < f1 && h == 0;) {
                     while (tab.off[l + 1] <= fa) ++l;
                     const int64_t fb = tab.off[l + 1] < f1 ? tab.off[l + 1] : f1;
                     if (n == kMaxPieces - 1) {
@@ -276,19 +307,25 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     fa = fb;
                 }
+                if (NH > 1 && h == 0) {
+                    volatile int32_t *hh = reinterpret_cast<volatile int32_t *>(head);
+                    hh[2] = n;
+                    hh[3] = (int32_t)row_bytes;
+                }
                 // the arrive (release) also publishes the piece table
-                mbar_expect_tx(full, row_bytes * (uint32_t)W + rbytes);
+                mbar_expect_tx(full, row_bytes * (uint32_t)WH + rbytes);
                 for (int i = 0; i < n; ++i) {
                     const int4 pc = pieces[i];
                     const int plo = pc.w & 0xffff, phi = pc.w >> 16;
                     if (pc.y < 0 || phi <= plo) continue;
                     const int64_t j = f0 + plo - pc.y - tab.off[pc.z];  // layer element at row plo
-                    for (int w = 0; w < W; ++w)
+                    for (int w = 0; w < WH; ++w)
                         bulk_g2s(smem_u32(st + ((size_t)w * ROW + (size_t)plo) * 2),
-                                 tab.ptr[w * L + pc.z] + j, (uint32_t)(phi - plo) * 2, full);
+                                 tab.ptr[(w0 + w) * L + pc.z] + j, (uint32_t)(phi - plo) * 2,
+                                 full);
                 }
             }
-            if (resid) bulk_g2s(smem_u32(st + gbytes), resid + f0, rbytes, full);
+            if (rbytes) bulk_g2s(smem_u32(st + gbytes), resid + f0, rbytes, full);
         };
         // Waits until the consumers have released the slot of iteration it.
         auto slot_free = [&](int it) {
@@ -299,35 +336,40 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
             return true;
         };
-        int it = 0;
+        int it = 0;  // stage iterations: NH per tile
         bool ok = true;
         unsigned long long q = 0;
         // the cyclic rounds: kept free of any other work, since the
         // producer's issue rate bounds the kernel's
-        for (; it < rounds_static; ++it) {
-            const int64_t t = blockIdx.x + (int64_t)it * G_;
+        for (int64_t r = 0; r < rounds_static && ok; ++r) {
+            const int64_t t = blockIdx.x + r * G_;
             if (t >= ntiles) break;
-            if (!slot_free(it)) {
-                ok = false;
-                break;
-            }
-            // the first tail index travels while the last cyclic tile's
-            // copies go out
-            if (dyn && it == rounds_static - 1) q = atomicAdd(dyn_next, 1ull);
-            issue(it % S, t);
-        }
-        // the tail, handed out one tile at a time; the next index travels
-        // while this tile's copies go out
-        if (ok && dyn) {
-            for (;; ++it) {
-                const int64_t t = rounds_static * G_ + (int64_t)q;
-                if (t >= ntiles) break;
+            for (int h = 0; h < NH; ++h, ++it) {
                 if (!slot_free(it)) {
                     ok = false;
                     break;
                 }
-                q = atomicAdd(dyn_next, 1ull);
-                issue(it % S, t);
+                // the first tail index travels while the last cyclic tile's
+                // copies go out
+                if (dyn && r == rounds_static - 1 && h == NH - 1) q = atomicAdd(dyn_next, 1ull);
+                issue(it % S, t, h);
+            }
+        }
+        // the tail, handed out one tile at a time; the next index travels
+        // while this tile's copies go out
+        if (ok && dyn) {
+            for (;;) {
+                const int64_t t = rounds_static * G_ + (int64_t)q;
+                if (t >= ntiles) break;
+                for (int h = 0; h < NH; ++h, ++it) {
+                    if (!slot_free(it)) {
+                        ok = false;
+                        break;
+                    }
+                    if (h == NH - 1) q = atomicAdd(dyn_next, 1ull);
+                    issue(it % S, t, h);
+                }
+                if (!ok) break;
             }
         }
         // no tile left: the consumers stop at this stage
@@ -356,6 +398,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 
     // consumers
+    // With worker halves (NH == 2) a warp sums the first half's workers of
+    // its group into part[] and adds the second half's subtree to it: for
+    // W = 16 that is the tree of all W (the binary-counter form joins the two
+    // subtrees of 8 leaves last), so the bits are unchanged.  TT = 2048 gives
+    // each warp one unit per tile, so one part[] per warp suffices.
+    constexpr int WTH = WT > 0 ? WT / NH : 0;
+    constexpr int MAXHH = NH == 1 ? MAXH : MAXH - 1;
+    float part[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) part[e] = 0.f;
     for (int it = 0;; ++it) {
         const int s = it % S;
         if (!mbar_wait(smem_u32(&bars[s]), (it / S) & 1, limit_ns)) {
@@ -363,8 +415,11 @@ __global__ void __launch_bounds__(kThreads, 1)
             return;
         }
         const unsigned char *st = stages + (size_t)s * sbytes;
-        const int64_t t = *reinterpret_cast<const volatile int64_t *>(st + sbytes - kStageHead);
-        if (t < 0) break;
+        const int64_t hdr = *reinterpret_cast<const volatile int64_t *>(st + sbytes - kStageHead);
+        if (hdr < 0) break;
+        const int64_t t = hdr / NH;
+        const int h = (int)(hdr - t * NH);
+        const bool last = h == NH - 1;  // the tile's last stage: finish the groups
         const int64_t f0 = f_begin + t * TT;
         const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
         for (int64_t lo = f0 + (int64_t)warp * FC_UNIT; lo < f1;
@@ -374,7 +429,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             float tss = 0.f;
             if (f < hi) {  // f + 8 <= hi: N and every unit start are multiples of 8
                 const size_t off = (size_t)(f - f0);
+                // with halves the residual comes from global memory: its load
+                // is issued before the tree, so that the two overlap
+                float4 g0 = make_float4(0.f, 0.f, 0.f, 0.f), g1 = g0;
+                if (NH > 1 && last && resid) {
+                    g0 = __ldcs(reinterpret_cast<const float4 *>(resid + f));
+                    g1 = __ldcs(reinterpret_cast<const float4 *>(resid + f + 4));
+                }
                 float a[8];
+                bool whole = false;  // a holds the tree of all W workers
                 if constexpr (!MIS) {
                     tree_sum<WT, MAXH, 8>(
                         W,
@@ -382,9 +445,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             unpack8(*reinterpret_cast<const uint4 *>(st + ((size_t)w * ROW + off) * 2), x);
                         },
                         a);
+                    whole = true;
                 } else {
                     const int uu = (int)off;
-                    const int4 *pieces = reinterpret_cast<const int4 *>(st + gbytes + (size_t)TT * 4);
+                    const int4 *pieces = reinterpret_cast<const int4 *>(st + gbytes + rreg);
                     int i = 0;
                     int4 pc = pieces[0];
                     while (pc.x <= uu) pc = pieces[++i];
@@ -397,8 +461,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (split == 8 && pc.y >= 0 && uu + pc.y >= alo && uu + pc.y + 8 <= ahi) {
                         // all 8 in one copied piece: two aligned loads, shifted
                         const int p0 = uu + (pc.y & ~7), d = pc.y & 7;
-                        tree_sum<WT, MAXH, 8>(
-                            W,
+                        tree_sum<WTH, MAXHH, 8>(
+                            WH,
                             [&](int w, float(&x)[8]) {
                                 const uint4 *q = reinterpret_cast<const uint4 *>(
                                     st + ((size_t)w * ROW + p0) * 2);
@@ -419,8 +483,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int j = 0; j < 4; ++j)
                             m[j] = 2 * j + 1 < split ? 0xffffffffu : (2 * j < split ? 0x0000ffffu : 0u);
-                        tree_sum<WT, MAXH, 8>(
-                            W,
+                        tree_sum<WTH, MAXHH, 8>(
+                            WH,
                             [&](int w, float(&x)[8]) {
                                 const unsigned char *row = st + (size_t)w * ROW * 2;
                                 const uint4 *qa = reinterpret_cast<const uint4 *>(row + (size_t)pa * 2);
@@ -439,40 +503,61 @@ __global__ void __launch_bounds__(kThreads, 1)
                         // unstaged pieces (a tile with more pieces than the
                         // table holds, or past the row's slack) or a group over
                         // three or more layers: element by element from
-                        // global memory
-                        int l = pc.z;
+                        // global memory, all W workers at the tile's last stage
+                        whole = true;
+                        if (last) {
+                            int l = pc.z;
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            while (tab.off[l + 1] <= f + e) ++l;
-                            const int64_t j = f + e - tab.off[l];
-                            float s1[1];
-                            tree_sum<WT, MAXH, 1>(
-                                W,
-                                [&](int w, float(&x)[1]) {
-                                    x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
-                                },
-                                s1);
-                            a[e] = s1[0];
+                            for (int e = 0; e < 8; ++e) {
+                                while (tab.off[l + 1] <= f + e) ++l;
+                                const int64_t j = f + e - tab.off[l];
+                                float s1[1];
+                                tree_sum<WT, MAXH, 1>(
+                                    W,
+                                    [&](int w, float(&x)[1]) {
+                                        x[0] = ld_half_as_float(tab.ptr[w * L + l] + j);
+                                    },
+                                    s1);
+                                a[e] = s1[0];
+                            }
                         }
                     }
                 }
-                float r[8];
-                if (resid) {
-                    const float4 *rr = reinterpret_cast<const float4 *>(st + gbytes + off * 4);
-                    const float4 r0 = rr[0], r1 = rr[1];
-                    r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
-                    r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
-                }
+                if (NH > 1 && !whole) {
+                    if (!last) {
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    a[e] = __fmul_rn(a[e], u);
-                    if (resid) a[e] = __fadd_rn(a[e], r[e]);
+                        for (int e = 0; e < 8; ++e) part[e] = a[e];
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) a[e] = __fadd_rn(part[e], a[e]);
+                    }
                 }
-                reinterpret_cast<float4 *>(out + f)[0] = make_float4(a[0], a[1], a[2], a[3]);
-                reinterpret_cast<float4 *>(out + f)[1] = make_float4(a[4], a[5], a[6], a[7]);
-                tss = __fadd_rn(tss, group_sumsq(a));
+                if (last) {
+                    float r[8];
+                    if (resid) {
+                        float4 r0, r1;
+                        if (NH == 1) {
+                            const float4 *rr = reinterpret_cast<const float4 *>(st + gbytes + off * 4);
+                            r0 = rr[0];
+                            r1 = rr[1];
+                        } else {
+                            r0 = g0;
+                            r1 = g1;
+                        }
+                        r[0] = r0.x; r[1] = r0.y; r[2] = r0.z; r[3] = r0.w;
+                        r[4] = r1.x; r[5] = r1.y; r[6] = r1.z; r[7] = r1.w;
+                    }
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) {
+                        a[e] = __fmul_rn(a[e], u);
+                        if (resid) a[e] = __fadd_rn(a[e], r[e]);
+                    }
+                    reinterpret_cast<float4 *>(out + f)[0] = make_float4(a[0], a[1], a[2], a[3]);
+                    reinterpret_cast<float4 *>(out + f)[1] = make_float4(a[4], a[5], a[6], a[7]);
+                    tss = __fadd_rn(tss, group_sumsq(a));
+                }
             }
-            if (partials) {
+            if (last && partials) {
                 tss = warp_sum_f32(tss);
                 if (lane == 0) partials[lo / FC_UNIT] = tss;
             }
@@ -482,19 +567,24 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// Tile size and stage count for W workers: a stage holds W rows of TT fp16
-// values (plus the slack of the shifted layout), TT fp32 residuals and the
-// piece table; about 64 KB of gradients, and as many stages as fit.
-static void tma_shape(int W, bool mis, int &TT, int &S, size_t &smem)
+// Tile size and stage count for W workers in NH stages per tile: a stage
+// holds W/NH rows of TT fp16 values (plus the slack of the shifted layout),
+// with one stage per tile also the TT fp32 residuals, and the piece table.
+// One stage per tile: about 64 KB of gradients, as many stages as fit in
+// one CTA per SM.  Two (worker halves): TT = 2048 (one unit per consumer
+// warp), as many stages as fit with two CTAs per SM.
+static void tma_shape(int W, bool mis, int NH, int &TT, int &S, size_t &smem)
 {
     TT = 2048;
-    while (TT > FC_UNIT && (size_t)W * TT * 2 > 65536) TT /= 2;
+    if (NH == 1)
+        while (TT > FC_UNIT && (size_t)W * TT * 2 > 65536) TT /= 2;
     const size_t row = (size_t)TT + (mis ? kSlack : 0);
-    const size_t sbytes = (size_t)W * row * 2 + (size_t)TT * 4 +
+    const size_t sbytes = (size_t)(W / NH) * row * 2 + (NH == 1 ? (size_t)TT * 4 : 0) +
                           (mis ? kMaxPieces * sizeof(int4) : 0) + kStageHead;
-    const size_t cap = 227 * 1024 - 128;
+    const size_t cap = (NH == 1 ? 227 : 113) * 1024 - 128;
+    const int smax = NH == 1 ? 4 : 6;
     S = (int)(cap / sbytes);
-    if (S > 4) S = 4;
+    if (S > smax) S = smax;
     smem = 128 + (size_t)S * sbytes;
 }
 
@@ -514,7 +604,7 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
     }
     int TT, S;
     size_t smem;
-    tma_shape(tab.W, !aligned, TT, S, smem);
+    tma_shape(tab.W, !aligned, 1, TT, S, smem);
     if (S < 2) return 0;
     if (!aligned) return 2;
     // Aligned layouts, by length (tiles of TT elements), as measured in
@@ -526,37 +616,61 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
     //  * short runs keep the aligned variant (2M x 16: 11 against 13 us).
     const int64_t tiles = (G.N + TT - 1) / TT;
     if (tiles >= FC_TMA_SHIFTED_MIN_TILES) {
-        tma_shape(tab.W, true, TT, S, smem);
+        tma_shape(tab.W, true, 1, TT, S, smem);
         if (S >= 2) return 2;
     }
     return tiles >= FC_TMA_REGISTER_MIN_TILES ? 0 : 1;
 }
 
-template <class Tab, int WT, int MAXH, bool MIS>
+// Worker halves (two stages per tile, two CTAs per SM) for the shifted
+// layout with 16 workers.
+#ifndef FC_TMA_HALVES
+#define FC_TMA_HALVES 1
+#endif
+
+template <class Tab, int WT, int MAXH, bool MIS, int NH>
 static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                                 const float *resid, float *out, float *partials,
                                 unsigned *ctr, cudaStream_t s, int64_t fb, int64_t fe)
 {
     int TT, S;
     size_t smem;
-    tma_shape(tab.W, MIS, TT, S, smem);
-    auto kern = k_reduce_tma<Tab, WT, MAXH, MIS>;
+    tma_shape(tab.W, MIS, NH, TT, S, smem);
+    auto kern = k_reduce_tma<Tab, WT, MAXH, MIS, NH>;
     static std::mutex mu;
-    static bool attr_set[64];
+    static int blocks[64];  // resident CTAs on the device (set on first use)
     int dev = 0;
     cudaGetDevice(&dev);
+    if (dev >= 64) return cudaErrorInvalidDevice;
+    int grid_cap = 0;
     {
         std::lock_guard<std::mutex> lock(mu);
-        if (dev < 64 && !attr_set[dev]) {
+        if (!blocks[dev]) {
             cudaError_t e = cudaFuncSetAttribute((const void *)kern,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 227 * 1024);
+                                                 (NH == 1 ? 227 : 113) * 1024);
             if (e != cudaSuccess) return e;
-            attr_set[dev] = true;
+            if (NH > 1) {
+                // two CTAs per SM need (nearly) all of its shared memory
+                e = cudaFuncSetAttribute((const void *)kern,
+                                         cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+                if (e != cudaSuccess) return e;
+                int sms = 0, per_sm = 0;
+                cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads,
+                                                                  smem) != cudaSuccess ||
+                    per_sm < 1)
+                    per_sm = 1;
+                blocks[dev] = (sms < 1 ? 1 : sms) * per_sm;
+            } else {
+                blocks[dev] = -1;
+            }
         }
+        grid_cap = blocks[dev];
     }
     const int64_t tiles = (fe - fb + TT - 1) / TT;
-    const int grid = grid_for((const void *)kern, kThreads, smem, tiles);
+    const int grid = grid_cap < 0 ? grid_for((const void *)kern, kThreads, smem, tiles)
+                                  : (int)(tiles < grid_cap ? (tiles < 1 ? 1 : tiles) : grid_cap);
     const int64_t drop = g_drop_tile.exchange(-1);
     const uint64_t limit = drop >= 0 ? g_drop_limit_ns.load() : kWaitLimitNs;
     return launch_after_prior(kern, (unsigned)grid, kThreads, smem, s, tab, G, TT, S, u,
@@ -568,10 +682,11 @@ static cudaError_t launch_tma_layout(const Tab &tab, const UnitGeom &G, float u,
                                      const float *resid, float *out, float *partials,
                                      unsigned *ctr, cudaStream_t s, int64_t fb, int64_t fe)
 {
+    constexpr int H = MIS && FC_TMA_HALVES ? 2 : 1;
     switch (tab.W) {
-    case 4: return launch_tma_w<Tab, 4, 3, MIS>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
-    case 8: return launch_tma_w<Tab, 8, 4, MIS>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
-    case 16: return launch_tma_w<Tab, 16, 5, MIS>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 4: return launch_tma_w<Tab, 4, 3, MIS, 1>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 8: return launch_tma_w<Tab, 8, 4, MIS, 1>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 16: return launch_tma_w<Tab, 16, 5, MIS, H>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
     default: break;
     }
     return cudaErrorNotSupported;
