@@ -1,7 +1,7 @@
 // Phase 1 (a2 + unit sums of squares) with TMA staging, for 4, 8 or 16
 // workers, N a multiple of 8 and a chunk size that is a multiple of 256.
 //
-// One CTA per SM (two with worker halves, below): a producer warp streams
+// One CTA per SM (two in the cases below): a producer warp streams
 // tiles of TT fused elements of all W workers (and the residual) from HBM
 // into a ring of S shared-memory stages with bulk copies (cp.async.bulk, completion counted on an mbarrier); eight
 // consumer warps take one 256-element unit each per tile, add the workers in
@@ -39,9 +39,11 @@
 // tree of 16 leaves those two subtrees are joined last, so the bits do not
 // change.  Two producers and sixteen consumer warps per SM: the GoogLeNet-
 // shaped phase 1 (many short layers, so many short copies per tile) went
-// from 55.0 to 51.7 us; the AlexNet-shaped one was unchanged (350 us), and
-// with 8 workers the halves gained nothing in phase 1 and lost 3 us in the
-// step, so 8 workers keep one stage per tile.
+// from 55.0 to 51.7 us; the AlexNet-shaped one was unchanged (350 us).
+// With 8 workers the halves gained nothing in phase 1 and lost 3 us in the
+// step; there two CTAs per SM keep whole stages instead (two 42 KB stages
+// each, 75 % carveout), which took the NiN-shaped phase 1 from 37.7 to
+// 34.1 us and its step from 68.7 to 66.8 us.
 //
 // Tile order: CTA b takes tiles b, b + grid, b + 2 grid, ...  In long
 // launches (kDynMinRounds rounds or more) that holds for all but the last
@@ -186,14 +188,14 @@ __device__ __forceinline__ int layer_shift(const Tab &tab, int l)
 // of producers that have finished with it (all zero between launches).
 // drop_tile >= 0 (test hook only, see fc_test_stage_loss): the producer
 // issues no copies for that tile, so the bounded waits on it run out.
-template <class Tab, int WT, int MAXH, bool MIS, int NH>
-__global__ void __launch_bounds__(kThreads, NH)
+template <class Tab, int WT, int MAXH, bool MIS, int NH, int CPS>
+__global__ void __launch_bounds__(kThreads, CPS)
     k_reduce_tma(const __grid_constant__ Tab tab, const UnitGeom G, const int TT,
                  const int S, const float u, const float *resid, float *out,
                  float *partials, unsigned *ctr, const int64_t drop_tile,
                  const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end)
 {
-    static_assert(NH == 1 || (MIS && WT == 16), "worker halves: shifted layout, 16 workers");
+    static_assert(NH == 1 || (MIS && WT == 16 && CPS == 2), "worker halves: shifted layout, 16 workers");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
     unsigned char *stages = smem + 128;
@@ -567,22 +569,26 @@ __global__ void __launch_bounds__(kThreads, NH)
     }
 }
 
-// Tile size and stage count for W workers in NH stages per tile: a stage
-// holds W/NH rows of TT fp16 values (plus the slack of the shifted layout),
-// with one stage per tile also the TT fp32 residuals, and the piece table.
-// One stage per tile: about 64 KB of gradients, as many stages as fit in
-// one CTA per SM.  Two (worker halves): TT = 2048 (one unit per consumer
-// warp), as many stages as fit with two CTAs per SM.
-static void tma_shape(int W, bool mis, int NH, int &TT, int &S, size_t &smem)
+// Tile size and stage count for W workers in NH stages per tile and CPS
+// CTAs per SM: a stage holds W/NH rows of TT fp16 values (plus the slack
+// of the shifted layout), with one stage per tile also the TT fp32
+// residuals, and the piece table.
+//  * one CTA per SM: about 64 KB of gradients a stage, as many stages as
+//    fit (at most 4);
+//  * worker halves (two CTAs per SM, full carveout): TT = 2048 (one unit per
+//    consumer warp), as many stages as fit in 113 KB (at most 6);
+//  * two CTAs per SM with whole stages (8 workers): TT = 2048, two stages,
+//    85 KB per CTA, so that a 75 % carveout holds both.
+static void tma_shape(int W, bool mis, int NH, int CPS, int &TT, int &S, size_t &smem)
 {
     TT = 2048;
-    if (NH == 1)
+    if (CPS == 1)
         while (TT > FC_UNIT && (size_t)W * TT * 2 > 65536) TT /= 2;
     const size_t row = (size_t)TT + (mis ? kSlack : 0);
     const size_t sbytes = (size_t)(W / NH) * row * 2 + (NH == 1 ? (size_t)TT * 4 : 0) +
                           (mis ? kMaxPieces * sizeof(int4) : 0) + kStageHead;
-    const size_t cap = (NH == 1 ? 227 : 113) * 1024 - 128;
-    const int smax = NH == 1 ? 4 : 6;
+    const size_t cap = CPS == 1 ? 227 * 1024 - 128 : NH > 1 ? 113 * 1024 - 128 : 86400 - 128;
+    const int smax = CPS == 1 ? 4 : NH > 1 ? 6 : 2;
     S = (int)(cap / sbytes);
     if (S > smax) S = smax;
     smem = 128 + (size_t)S * sbytes;
@@ -604,7 +610,7 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
     }
     int TT, S;
     size_t smem;
-    tma_shape(tab.W, !aligned, 1, TT, S, smem);
+    tma_shape(tab.W, !aligned, 1, 1, TT, S, smem);
     if (S < 2) return 0;
     if (!aligned) return 2;
     // Aligned layouts, by length (tiles of TT elements), as measured in
@@ -616,27 +622,31 @@ int tma_layout(const Tab &tab, const UnitGeom &G, const float *partials)
     //  * short runs keep the aligned variant (2M x 16: 11 against 13 us).
     const int64_t tiles = (G.N + TT - 1) / TT;
     if (tiles >= FC_TMA_SHIFTED_MIN_TILES) {
-        tma_shape(tab.W, true, 1, TT, S, smem);
+        tma_shape(tab.W, true, 1, 1, TT, S, smem);
         if (S >= 2) return 2;
     }
     return tiles >= FC_TMA_REGISTER_MIN_TILES ? 0 : 1;
 }
 
 // Worker halves (two stages per tile, two CTAs per SM) for the shifted
-// layout with 16 workers.
+// layout with 16 workers; two CTAs per SM with whole stages for the shifted
+// layout with 8 workers.
 #ifndef FC_TMA_HALVES
 #define FC_TMA_HALVES 1
 #endif
+#ifndef FC_TMA_W8_PAIRS
+#define FC_TMA_W8_PAIRS 1
+#endif
 
-template <class Tab, int WT, int MAXH, bool MIS, int NH>
+template <class Tab, int WT, int MAXH, bool MIS, int NH, int CPS>
 static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
                                 const float *resid, float *out, float *partials,
                                 unsigned *ctr, cudaStream_t s, int64_t fb, int64_t fe)
 {
     int TT, S;
     size_t smem;
-    tma_shape(tab.W, MIS, NH, TT, S, smem);
-    auto kern = k_reduce_tma<Tab, WT, MAXH, MIS, NH>;
+    tma_shape(tab.W, MIS, NH, CPS, TT, S, smem);
+    auto kern = k_reduce_tma<Tab, WT, MAXH, MIS, NH, CPS>;
     static std::mutex mu;
     static int blocks[64];  // resident CTAs on the device (set on first use)
     int dev = 0;
@@ -648,12 +658,13 @@ static cudaError_t launch_tma_w(const Tab &tab, const UnitGeom &G, float u,
         if (!blocks[dev]) {
             cudaError_t e = cudaFuncSetAttribute((const void *)kern,
                                                  cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                 (NH == 1 ? 227 : 113) * 1024);
+                                                 CPS == 1 ? 227 * 1024 : (int)smem);
             if (e != cudaSuccess) return e;
-            if (NH > 1) {
-                // two CTAs per SM need (nearly) all of its shared memory
+            if (CPS > 1) {
+                // two CTAs per SM: the carveout that holds both
                 e = cudaFuncSetAttribute((const void *)kern,
-                                         cudaFuncAttributePreferredSharedMemoryCarveout, 100);
+                                         cudaFuncAttributePreferredSharedMemoryCarveout,
+                                         NH > 1 ? 100 : 75);
                 if (e != cudaSuccess) return e;
                 int sms = 0, per_sm = 0;
                 cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -683,10 +694,11 @@ static cudaError_t launch_tma_layout(const Tab &tab, const UnitGeom &G, float u,
                                      unsigned *ctr, cudaStream_t s, int64_t fb, int64_t fe)
 {
     constexpr int H = MIS && FC_TMA_HALVES ? 2 : 1;
+    constexpr int P8 = MIS && FC_TMA_W8_PAIRS ? 2 : 1;
     switch (tab.W) {
-    case 4: return launch_tma_w<Tab, 4, 3, MIS, 1>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
-    case 8: return launch_tma_w<Tab, 8, 4, MIS, 1>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
-    case 16: return launch_tma_w<Tab, 16, 5, MIS, H>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 4: return launch_tma_w<Tab, 4, 3, MIS, 1, 1>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 8: return launch_tma_w<Tab, 8, 4, MIS, 1, P8>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
+    case 16: return launch_tma_w<Tab, 16, 5, MIS, H, H>(tab, G, u, resid, out, partials, ctr, s, fb, fe);
     default: break;
     }
     return cudaErrorNotSupported;
