@@ -1,14 +1,15 @@
 // Phase 1 (a2 + unit sums of squares) with TMA staging, for 4, 8 or 16
 // workers, N a multiple of 8 and a chunk size that is a multiple of 256.
 //
-// One CTA per SM (two in the cases below): a producer warp streams
-// tiles of TT fused elements of all W workers (and the residual) from HBM
-// into a ring of S shared-memory stages with bulk copies (cp.async.bulk, completion counted on an mbarrier); eight
-// consumer warps take one 256-element unit each per tile, add the workers in
-// the same binary tree as the register kernel (k_reduce) from shared memory,
-// and write `a` and the unit sums of squares exactly as k_reduce does, so the
-// results are bit-identical.  The copies keep S-1 tiles of every worker in
-// flight per SM regardless of register pressure.
+// One CTA per SM (two in the cases below): a producer warp streams tiles
+// of TT fused elements of all W workers (and the residual) from HBM into a
+// ring of S shared-memory stages with bulk copies (cp.async.bulk, completion
+// counted on an mbarrier); eight consumer warps take one 256-element unit
+// each per tile, add the workers in the same binary tree as the register
+// kernel (k_reduce) from shared memory, and write `a` and the unit sums of
+// squares exactly as k_reduce does, so the results are bit-identical.  The
+// copies keep S-1 tiles of every worker in flight per SM regardless of
+// register pressure.
 //
 // Two layouts:
 //  * aligned (MIS = false): every layer starts at a multiple of 8 fused
@@ -234,18 +235,80 @@ __global__ void __launch_bounds__(kThreads, CPS)
     if (warp == kConsumerWarps) {
         // producer
         if (lane != 0) return;
-        // Fills stage s with worker half h of tile t (its index and half
-        // first, for the consumers).
-        auto issue = [&](int s, int64_t t, int h) {
-            const uint32_t full = smem_u32(&bars[s]);
+        // Plans stage s for worker half h of tile t: the tile's index and half
+        // (for the consumers) and, in the shifted layout, the piece table, with
+        // its length and the bytes it copies per worker row.
+        //
+        // Piece table: {end of the piece (tile-relative), sh (or -1 if
+        // unstaged), layer, copied range [lo, hi) of the row as lo | hi << 16}.
+        // The last entry always ends at the tile's end.  The second half of a
+        // tile copies the first half's table (the stage planned just before).
+        auto plan = [&](int s, int64_t t, int h) {
             unsigned char *st = stages + (size_t)s * sbytes;
             volatile int64_t *head = reinterpret_cast<volatile int64_t *>(st + sbytes - kStageHead);
             head[0] = t * NH + h;
+            if constexpr (MIS) {
+                volatile int32_t *hh = reinterpret_cast<volatile int32_t *>(head);
+                int4 *pieces = reinterpret_cast<int4 *>(st + gbytes + rreg);
+                if (h > 0) {
+                    const unsigned char *pst = stages + (size_t)((s + S - 1) % S) * sbytes;
+                    const volatile int32_t *ph =
+                        reinterpret_cast<const volatile int32_t *>(pst + sbytes - kStageHead);
+                    const int n = ph[2];
+                    const int4 *pp = reinterpret_cast<const int4 *>(pst + gbytes + rreg);
+                    for (int i = 0; i < n; ++i) pieces[i] = pp[i];
+                    hh[2] = n;
+                    hh[3] = ph[3];
+                    return;
+                }
+                const int64_t f0 = f_begin + t * TT;
+                const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
+                int n = 0;
+                uint32_t row_bytes = 0;
+                int64_t prev_phi = 0;  // end of the last staged piece's frames
+                int l = find_layer(tab, f0);
+                for (int64_t fa = f0; fa < f1;) {
+                    while (tab.off[l + 1] <= fa) ++l;
+                    const int64_t fb = tab.off[l + 1] < f1 ? tab.off[l + 1] : f1;
+                    if (n == kMaxPieces - 1) {
+                        pieces[n++] = make_int4((int)(f1 - f0), -1, l, 0);
+                        break;
+                    }
+                    // The piece is copied as the whole 16-byte frames that hold
+                    // it, including the partial frames at a layer's ends (every
+                    // frame holds at least one element of the layer, so no copy
+                    // reaches a page the layer does not touch).  Its gap is the
+                    // smallest multiple of 8 that puts its first frame after the
+                    // last frame of the piece before.
+                    const int d = layer_shift(tab, l);
+                    const int64_t x = fa - f0;
+                    int64_t g = prev_phi - round_down8(x + d);
+                    g = g > 0 ? round_up8(g) : 0;
+                    const int64_t sh = g + d;
+                    const int64_t plo = round_down8(x + sh);
+                    const int64_t phi = round_up8(fb - f0 + sh);
+                    if (phi > ROW) {
+                        pieces[n++] = make_int4((int)(fb - f0), -1, l, 0);
+                    } else {
+                        pieces[n++] = make_int4((int)(fb - f0), (int)sh, l, (int)(plo | (phi << 16)));
+                        row_bytes += (uint32_t)(phi - plo) * 2;
+                        prev_phi = phi;
+                    }
+                    fa = fb;
+                }
+                hh[2] = n;
+                hh[3] = (int32_t)row_bytes;
+            }
+        };
+        // Issues the copies of stage s, planned for worker half h of tile t;
+        // the expect-tx arrive (a release) also publishes the plan.
+        auto issue = [&](int s, int64_t t, int h) {
+            const uint32_t full = smem_u32(&bars[s]);
+            unsigned char *st = stages + (size_t)s * sbytes;
             if (t == drop_tile) return;
             const int64_t f0 = f_begin + t * TT;
             const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
             const uint32_t rbytes = NH == 1 && resid ? (uint32_t)((f1 - f0) * 4) : 0u;
-            const int w0 = h * WH;
             if constexpr (!MIS) {
                 mbar_expect_tx(full, (uint32_t)((f1 - f0) * 2 * W) + rbytes);
                 int l = find_layer(tab, f0);
@@ -259,62 +322,12 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     fa = fb;
                 }
             } else {
-                // Piece table: {end of the piece (tile-relative), sh (or -1
-                // if unstaged), layer, copied range [lo, hi) of the row as
-                // lo | hi << 16}.  The last entry always ends at the tile's end.
-                // The second half of a tile copies the first half's table
-                // (the stage issued just before), with its count and row bytes
-                // from that stage's head.
-                int4 *pieces = reinterpret_cast<int4 *>(st + gbytes + rreg);
-                int n = 0;
-                uint32_t row_bytes = 0;
-                if (h > 0) {
-                    const unsigned char *pst = stages + (size_t)((s + S - 1) % S) * sbytes;
-                    const volatile int32_t *ph =
-                        reinterpret_cast<const volatile int32_t *>(pst + sbytes - kStageHead);
-                    n = ph[2];
-                    row_bytes = (uint32_t)ph[3];
-                    const int4 *pp = reinterpret_cast<const int4 *>(pst + gbytes + rreg);
-                    for (int i = 0; i < n; ++i) pieces[i] = pp[i];
-                }
-                int64_t prev_phi = 0;  // end of the last staged piece's frames
-                int l = find_layer(tab, f0);
-                for (int64_t fa = f0; fa < f1 && h == 0;) {
-                    while (tab.off[l + 1] <= fa) ++l;
-                    const int64_t fb = tab.off[l + 1] < f1 ? tab.off[l + 1] : f1;
-                    if (n == kMaxPieces - 1) {
-                        pieces[n++] = make_int4((int)(f1 - f0), -1, l, 0);
-                        break;
-                    }
-                    // The piece is copied as the whole 16-byte frames that
-                    // hold it, including the partial frames at a layer's ends
-                    // (every frame holds at least one element of the layer,
-                    // so no copy reaches a page the layer does not touch).
-                    // Its gap is the smallest multiple of 8 that puts its
-                    // first frame after the last frame of the piece before.
-                    const int d = layer_shift(tab, l);
-                    const int64_t x = fa - f0;
-                    int64_t g = prev_phi - round_down8(x + d);
-                    g = g > 0 ? round_up8(g) : 0;
-                    const int64_t sh = g + d;
-                    const int64_t plo = round_down8(x + sh);
-                    const int64_t phi = round_up8(fb - f0 + sh);
-                    if (phi > ROW) {
-                        pieces[n++] = make_int4((int)(fb - f0), -1, l, 0);
-                    } else {
-                        pieces[n++] = make_int4((int)(fb - f0), (int)sh, l,
-                                                (int)(plo | (phi << 16)));
-                        row_bytes += (uint32_t)(phi - plo) * 2;
-                        prev_phi = phi;
-                    }
-                    fa = fb;
-                }
-                if (NH > 1 && h == 0) {
-                    volatile int32_t *hh = reinterpret_cast<volatile int32_t *>(head);
-                    hh[2] = n;
-                    hh[3] = (int32_t)row_bytes;
-                }
-                // the arrive (release) also publishes the piece table
+                const volatile int32_t *hh =
+                    reinterpret_cast<const volatile int32_t *>(st + sbytes - kStageHead);
+                const int n = hh[2];
+                const uint32_t row_bytes = (uint32_t)hh[3];
+                const int4 *pieces = reinterpret_cast<const int4 *>(st + gbytes + rreg);
+                const int w0 = h * WH;
                 mbar_expect_tx(full, row_bytes * (uint32_t)WH + rbytes);
                 for (int i = 0; i < n; ++i) {
                     const int4 pc = pieces[i];
@@ -351,6 +364,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     ok = false;
                     break;
                 }
+                plan(it % S, t, h);
                 // the first tail index travels while the last cyclic tile's
                 // copies go out
                 if (dyn && r == rounds_static - 1 && h == NH - 1) q = atomicAdd(dyn_next, 1ull);
@@ -368,6 +382,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
                         ok = false;
                         break;
                     }
+                    plan(it % S, t, h);
                     if (h == NH - 1) q = atomicAdd(dyn_next, 1ull);
                     issue(it % S, t, h);
                 }
