@@ -163,18 +163,19 @@ __global__ void __launch_bounds__(SEL_THREADS)
             const float n = chunk_norm_from_units(G, partials, c, lane);
             if (lane == 0) norms[c] = n;
         }
-        // publish this block's norms before counting it: the barrier orders
-        // every warp's writes before thread 0's fence, which makes them
-        // visible device-wide before the count
+        // Publish this block's norms before counting it: the barrier orders
+        // every warp's writes before thread 0's count, whose release makes
+        // them visible device-wide with it; its acquire makes every earlier
+        // block's norms visible to the block that counts last.
         __syncthreads();
         if (tid == 0) {
-            __threadfence();
-            const unsigned seen = atomicAdd(done, 1u);
+            unsigned seen;
+            asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;"
+                         : "=r"(seen)
+                         : "l"(done)
+                         : "memory");
             s_last = seen == gridDim.x - 1 ? 1u : 0u;
-            if (s_last) {
-                __threadfence();  // every block's norms, before this block reads them
-                *done = 0u;       // ready for the next call
-            }
+            if (s_last) *done = 0u;  // ready for the next call
         }
         __syncthreads();
         if (!s_last) return;
@@ -200,7 +201,19 @@ __global__ void __launch_bounds__(SEL_THREADS)
 
     const bool in_smem = C <= SEL_SMEM_KEYS;
     if (in_smem) {
-        for (int64_t c = tid; c < C; c += SEL_THREADS) skeys[c] = __float_as_uint(__ldcg(norms + c));
+        // all of a thread's loads in flight before its first store
+        constexpr int R = (SEL_SMEM_KEYS + SEL_THREADS - 1) / SEL_THREADS;
+        uint32_t v[R];
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int64_t c = tid + (int64_t)i * SEL_THREADS;
+            v[i] = c < C ? __float_as_uint(__ldcg(norms + c)) : 0u;
+        }
+#pragma unroll
+        for (int i = 0; i < R; ++i) {
+            const int64_t c = tid + (int64_t)i * SEL_THREADS;
+            if (c < C) skeys[c] = v[i];
+        }
         __syncthreads();
     }
     auto key_at = [&](int64_t c) -> uint32_t {
