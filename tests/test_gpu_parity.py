@@ -485,6 +485,48 @@ def test_select_with_only_the_fp16_send_buffer():
     assert bits_equal(p16.cpu().numpy().view(np.uint16), oracle.pack_fp16(packed_o, wl.loss_scale))
 
 
+def _norm_patterns(kind, C, rng):
+    """Non-negative finite binary32 norms whose bit patterns agree above a
+    chosen bit: the radix select's digits are then constant in its first
+    passes and spread only in the last ones (or, for "wide", from the
+    first)."""
+    if kind == "low5":        # differ in bits 4..0 only
+        bits = 0x3F800000 + rng.integers(0, 32, C)
+    elif kind == "low20":     # differ in bits 19..0
+        bits = 0x3C500000 + rng.integers(0, 1 << 20, C)
+    elif kind == "wide":      # every exponent from 2^-126 up
+        bits = rng.integers(0x00800000, 0x7F000000, C)
+    elif kind == "equal":     # all keys the same
+        bits = np.full(C, 0x3E4CCCCD)
+    elif kind == "two":       # two values in bit 0 only, many ties at tau
+        bits = 0x3F000000 + (rng.random(C) < 0.5)
+    else:
+        raise ValueError(kind)
+    return np.asarray(bits, dtype=np.uint32).view(np.float32)
+
+
+@pytest.mark.parametrize("kind", ["low5", "low20", "wide", "equal", "two"])
+@pytest.mark.parametrize("C", [1, 37, 1904, 11264, 11265])
+def test_select_on_norms_sharing_leading_bits(kind, C):
+    """fc_chunk_select against the oracle's selection on norms that share
+    their leading bits, for k = 1, 30 %, C - 1 and C: kept set, index list
+    and threshold exact.  C = 11,265 keys are more than the selection holds
+    in shared memory, so they are read from global memory."""
+    rng = np.random.default_rng(300 + C + len(kind))
+    norms_np = _norm_patterns(kind, C, rng)
+    norms = torch.from_numpy(norms_np).cuda()
+    for k in sorted({1, max(1, (3 * C) // 10), max(1, C - 1), C}):
+        idx_o, mask_o, _, thr_o = oracle.chunk_select(norms_np, k)
+        idx = torch.empty(k, dtype=torch.int32, device="cuda")
+        mask = torch.empty(C, dtype=torch.uint8, device="cuda")
+        thr = torch.empty(1, dtype=torch.float32, device="cuda")
+        fc.fc_chunk_select(norms, C, k, None, C, 1, idx, mask, None, thr)
+        torch.cuda.synchronize()
+        assert np.array_equal(idx.cpu().numpy(), idx_o), (kind, C, k)
+        assert np.array_equal(mask.cpu().numpy(), mask_o), (kind, C, k)
+        assert bits_equal(thr.cpu().numpy(), np.asarray(thr_o, np.float32).reshape(1)), (kind, C, k)
+
+
 @pytest.mark.parametrize("inplace", [False, True], ids=["separate_a", "inplace"])
 @pytest.mark.parametrize("sizes,kind", [
     ([8192, 16384, 40960], fc.FC_REDUCE_STAGED),
