@@ -116,12 +116,15 @@ def test_shifted_layout_odd_layer_sizes():
         _run_workload(wl, expect_kernel=fc.FC_REDUCE_STAGED_SHIFTED)
 
 
-def test_shifted_layout_many_tiny_layers():
+@pytest.mark.parametrize("W,L,cid", [(8, 300, 163), (16, 190, 167)])
+def test_shifted_layout_many_tiny_layers(W, L, cid):
     """Hundreds of 1..20-element layers: tiles with more pieces than the
-    stage's piece table, whose rest is read from global memory."""
+    stage's piece table, whose rest is read from global memory (with 16
+    workers, at the second of the tile's two stages).  L stays within
+    FC_MAX_TABLE_PTRS worker-layer pointers."""
     rng = np.random.default_rng(8)
-    sizes = _sizes_n8(rng.integers(1, 21, 300))
-    wl = workload.custom(W=8, sizes=sizes, chunk=256, keep_percent=30, config_id=163, steps=2)
+    sizes = _sizes_n8(rng.integers(1, 21, L))
+    wl = workload.custom(W=W, sizes=sizes, chunk=256, keep_percent=30, config_id=cid, steps=2)
     _run_workload(wl, expect_kernel=fc.FC_REDUCE_STAGED_SHIFTED)
 
 
