@@ -341,6 +341,12 @@ __global__ void __launch_bounds__(kThreads, CPS)
                 }
             }
             if (rbytes) bulk_g2s(smem_u32(st + gbytes), resid + f0, rbytes, full);
+            // with halves the consumers read the residual themselves, at the
+            // tile's second stage: warm L2 with it at the first
+            if (NH > 1 && h == 0 && resid)
+                asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(resid + f0),
+                             "r"((uint32_t)((f1 - f0) * 4))
+                             : "memory");
         };
         // Waits until the consumers have released the slot of iteration it.
         auto slot_free = [&](int it) {
