@@ -26,25 +26,28 @@
 //    of every piece (running past the tile's ends where the layer goes on)
 //    and records the pieces in a small table in the stage.  A consumer reads
 //    its 8 elements with two 16-byte shared-memory loads and a funnel shift;
-//    only groups not fully inside one copied piece (at layer boundaries)
-//    read their elements from global memory.  Aligned layouts long enough
-//    (FC_TMA_SHIFTED_MIN_TILES) also take this variant, with every shift 0:
-//    it measured faster on long runs.  Aligned mid-size runs go to the
-//    register kernel instead (see tma_layout).
+//    a group across a layer boundary takes each part from its own staged
+//    piece, and only groups in unstaged pieces (past the table or the row's
+//    slack) or across three or more layers read their elements from global
+//    memory.  Aligned layouts long enough (FC_TMA_SHIFTED_MIN_TILES) also
+//    take this variant, with every shift 0: it measured faster on long
+//    runs.  Aligned mid-size runs go to the register kernel instead (see
+//    tma_layout).
 //
 // Worker halves (shifted layout, 16 workers): each tile goes through the
 // ring as two stages, the first holding workers 0..7 and the second workers
-// 8..15, with two CTAs per SM (each about 100 KB of stages, residual read
-// by the consumers from global memory).  A consumer warp keeps the first
-// half's subtree in registers and adds the second's to it: in the binary
-// tree of 16 leaves those two subtrees are joined last, so the bits do not
-// change.  Two producers and sixteen consumer warps per SM: the GoogLeNet-
-// shaped phase 1 (many short layers, so many short copies per tile) went
-// from 55.0 to 51.7 us; the AlexNet-shaped one was unchanged (350 us).
-// With 8 workers the halves gained nothing in phase 1 and lost 3 us in the
-// step; there two CTAs per SM keep whole stages instead (two 42 KB stages
-// each, 75 % carveout), which took the NiN-shaped phase 1 from 37.7 to
-// 34.1 us and its step from 68.7 to 66.8 us.
+// 8..15, with two CTAs per SM (each about 100 KB of stages; the residual is
+// prefetched into L2 at the first stage and read by the consumers from
+// there at the second).  A consumer warp keeps the first half's subtree in
+// registers and adds the second's to it: in the binary tree of 16 leaves
+// those two subtrees are joined last, so the bits do not change.  Two
+// producers and sixteen consumer warps per SM: the GoogLeNet-shaped phase 1
+// (many short layers, so many short copies per tile) went from 55.0 to
+// 51.7 us; the AlexNet-shaped one was unchanged (350 us).  With 8 workers
+// the halves gained nothing in phase 1 and lost 3 us in the step; there two
+// CTAs per SM keep whole stages instead (two 42 KB stages each, 75 %
+// carveout), which took the NiN-shaped phase 1 from 37.7 to 34.1 us and its
+// step from 68.7 to 66.8 us.
 //
 // Tile order: CTA b takes tiles b, b + grid, b + 2 grid, ...  In long
 // launches (kDynMinRounds rounds or more) that holds for all but the last
