@@ -199,7 +199,8 @@ __global__ void __launch_bounds__(kThreads, CPS)
                  float *partials, unsigned *ctr, const int64_t drop_tile,
                  const uint64_t limit_ns, const int64_t f_begin, const int64_t f_end)
 {
-    static_assert(NH == 1 || (MIS && WT == 16 && CPS == 2), "worker halves: shifted layout, 16 workers");
+    static_assert(NH == 1 || (MIS && WT == 16 && CPS == 2),
+                  "worker halves: shifted layout, 16 workers, two CTAs per SM");
     extern __shared__ __align__(128) unsigned char smem[];
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem);  // full[S], empty[S]
     unsigned char *stages = smem + 128;
@@ -212,7 +213,7 @@ __global__ void __launch_bounds__(kThreads, CPS)
     const int ROW = TT + (MIS ? kSlack : 0);  // elements per worker row
     const size_t gbytes = (size_t)WH * ROW * 2;
     // with one stage per tile the residual is staged too; with halves the
-    // consumers read it from global memory
+    // consumers read it from global memory (prefetched into L2)
     const size_t rreg = NH == 1 ? (size_t)TT * 4 : 0;
     const size_t sbytes = gbytes + rreg + (MIS ? kMaxPieces * sizeof(int4) : 0) + kStageHead;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
