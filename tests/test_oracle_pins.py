@@ -147,6 +147,31 @@ def test_tree_reduce_exact_integer_sums_and_unscale():
                 assert abs(float(a[i]) - float(exact)) <= abs(float(exact)) * 2 ** -23
 
 
+def _round_f32(x: Fraction) -> float:
+    """The binary32 value nearest a positive rational in the normal range
+    (ties to even), from the format's definition: 24 significant bits."""
+    e = x.numerator.bit_length() - x.denominator.bit_length()
+    if Fraction(2) ** e > x:
+        e -= 1
+    scale = Fraction(2) ** (e - 23)               # one unit in the last place
+    m = x / scale                                 # in [2^23, 2^24)
+    q, r = divmod(m.numerator, m.denominator)
+    rem = Fraction(r, m.denominator)
+    if rem > Fraction(1, 2) or (rem == Fraction(1, 2) and q % 2 == 1):
+        q += 1
+    return float(q * scale)
+
+
+def test_unscale_factor_is_the_nearest_binary32_to_one_over_s_w():
+    """u = 1/(S*W) rounded once to binary32, also where S*W is not a power
+    of two; S is the binary32 loss scale the calls take (1e-3 is first
+    rounded to binary32)."""
+    for S, W in [(1000.0, 3), (1024.0, 5), (512.0, 7), (65536.0, 6), (0.5, 3), (128.0, 96),
+                 (3.0, 11), (1e-3, 13), (4096.0, 1), (256.0, 16)]:
+        want = _round_f32(1 / (Fraction(float(np.float32(S))) * W))
+        assert float(oracle.unscale_factor(S, W)) == want, (S, W)
+
+
 def test_tree_reduce_worker_index_and_residual():
     # worker w contributes only element w: a transposed operand would fail
     W, N = 4, 4
