@@ -32,6 +32,7 @@
  * header says otherwise.
  */
 #include <math.h>
+#include <stdatomic.h>
 #include <stdint.h>
 #include <stdlib.h>
 #include <string.h>
@@ -147,12 +148,20 @@ void orc_tree_reduce(int32_t W, int64_t N, const uint16_t *fused,
                      float loss_scale, const float *residual, float *out)
 {
     /* orc_half_to_float of every bit pattern, looked up instead of
-     * recomputed per element (the values are identical). */
+     * recomputed per element (the values are identical).  The table is
+     * filled once, by the first caller; a concurrent caller waits until it
+     * is complete (state 0 empty, 1 being filled, 2 ready). */
     static float h2f[65536];
-    static int h2f_ready = 0;
-    if (!h2f_ready) {
-        for (int b = 0; b < 65536; ++b) h2f[b] = orc_half_to_float((uint16_t)b);
-        h2f_ready = 1;
+    static atomic_int h2f_state = 0;
+    if (atomic_load_explicit(&h2f_state, memory_order_acquire) != 2) {
+        int expected = 0;
+        if (atomic_compare_exchange_strong(&h2f_state, &expected, 1)) {
+            for (int b = 0; b < 65536; ++b) h2f[b] = orc_half_to_float((uint16_t)b);
+            atomic_store_explicit(&h2f_state, 2, memory_order_release);
+        } else {
+            while (atomic_load_explicit(&h2f_state, memory_order_acquire) != 2) {
+            }
+        }
     }
     float *x = (float *)malloc(sizeof(float) * (size_t)W);
     float inv = orc_unscale_factor(loss_scale, W);
