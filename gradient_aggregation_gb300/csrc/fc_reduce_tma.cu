@@ -313,16 +313,25 @@ __global__ void __launch_bounds__(kThreads, CPS)
             const int64_t f0 = f_begin + t * TT;
             const int64_t f1 = f0 + TT < f_end ? f0 + TT : f_end;
             const uint32_t rbytes = NH == 1 && resid ? (uint32_t)((f1 - f0) * 4) : 0u;
+            // The copies' sources are read from the parameter bank into
+            // registers before the first copy of a piece is issued: a copy
+            // (an asm with a memory clobber) would otherwise hold each
+            // pointer's read back until the copy before it has gone out.
+            constexpr int WHc = WT / NH;
             if constexpr (!MIS) {
                 mbar_expect_tx(full, (uint32_t)((f1 - f0) * 2 * W) + rbytes);
                 int l = find_layer(tab, f0);
                 for (int64_t fa = f0; fa < f1;) {
                     while (tab.off[l + 1] <= fa) ++l;
                     const int64_t fb = tab.off[l + 1] < f1 ? tab.off[l + 1] : f1;
-                    for (int w = 0; w < W; ++w)
+                    const int64_t j = fa - tab.off[l];
+                    const __half *src[WHc];
+#pragma unroll
+                    for (int w = 0; w < WHc; ++w) src[w] = tab.ptr[w * L + l];
+#pragma unroll
+                    for (int w = 0; w < WHc; ++w)
                         bulk_g2s(smem_u32(st + ((size_t)w * ROW + (size_t)(fa - f0)) * 2),
-                                 tab.ptr[w * L + l] + (fa - tab.off[l]),
-                                 (uint32_t)((fb - fa) * 2), full);
+                                 src[w] + j, (uint32_t)((fb - fa) * 2), full);
                     fa = fb;
                 }
             } else {
@@ -338,10 +347,13 @@ __global__ void __launch_bounds__(kThreads, CPS)
                     const int plo = pc.w & 0xffff, phi = pc.w >> 16;
                     if (pc.y < 0 || phi <= plo) continue;
                     const int64_t j = f0 + plo - pc.y - tab.off[pc.z];  // layer element at row plo
-                    for (int w = 0; w < WH; ++w)
-                        bulk_g2s(smem_u32(st + ((size_t)w * ROW + (size_t)plo) * 2),
-                                 tab.ptr[(w0 + w) * L + pc.z] + j, (uint32_t)(phi - plo) * 2,
-                                 full);
+                    const __half *src[WHc];
+#pragma unroll
+                    for (int w = 0; w < WHc; ++w) src[w] = tab.ptr[(w0 + w) * L + pc.z];
+#pragma unroll
+                    for (int w = 0; w < WHc; ++w)
+                        bulk_g2s(smem_u32(st + ((size_t)w * ROW + (size_t)plo) * 2), src[w] + j,
+                                 (uint32_t)(phi - plo) * 2, full);
                 }
             }
             if (rbytes) bulk_g2s(smem_u32(st + gbytes), resid + f0, rbytes, full);
