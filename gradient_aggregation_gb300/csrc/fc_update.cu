@@ -141,7 +141,13 @@ cudaError_t launch_update(const TileGeom &G, int64_t tiles, const float *a,
                           __half *w16, bool inplace, cudaStream_t s,
                           const unsigned *status)
 {
-    const int grid = grid_for((const void *)k_update, FC_UPDATE_BLOCK, 0, tiles);
+    int grid = grid_for((const void *)k_update, FC_UPDATE_BLOCK, 0, tiles);
+    // as many rounds of tiles as the resident blocks need, dealt out evenly
+    // (the last round as full as the others)
+    if (tiles > grid) {
+        const int64_t rounds = (tiles + grid - 1) / grid;
+        grid = (int)((tiles + rounds - 1) / rounds);
+    }
     return launch_after_prior(k_update, (unsigned)grid, FC_UPDATE_BLOCK, 0, s, G, tiles,
                               a, mask, slot, packed, packed16, send_scale, lr,
                               mu, r, v, w, w16, inplace ? 1 : 0, status);
