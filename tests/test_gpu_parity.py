@@ -531,18 +531,22 @@ def test_select_on_norms_sharing_leading_bits(kind, C):
 
 
 @pytest.mark.parametrize("inplace", [False, True], ids=["separate_a", "inplace"])
-@pytest.mark.parametrize("sizes,kind", [
-    ([8192, 16384, 40960], fc.FC_REDUCE_STAGED),
-    ([8191, 16385, 40960], fc.FC_REDUCE_STAGED_SHIFTED)], ids=["aligned", "shifted"])
-def test_staged_reduction_reports_a_wait_that_runs_out(sizes, kind, inplace):
+@pytest.mark.parametrize("W,sizes,kind", [
+    (16, [8192, 16384, 40960], fc.FC_REDUCE_STAGED),
+    (16, [8191, 16385, 40960], fc.FC_REDUCE_STAGED_SHIFTED),
+    (8, [8191, 16385, 40960], fc.FC_REDUCE_STAGED_SHIFTED)],
+    ids=["aligned", "shifted", "shifted_w8"])
+def test_staged_reduction_reports_a_wait_that_runs_out(W, sizes, kind, inplace):
     """Failure path of the TMA-staged reduction, without any fault: the test
     hook makes the next launch issue no copies for tile 0, so the waits on it
     run out (20 ms limit).  The step reports it (NaN threshold, nothing kept,
     idx -1, FC_ERR_TIMEOUT from fc_step_status) and is not applied: velocity,
     weights and the fp16 weights keep their bits, and with a separate `a`
     buffer so does the residual, so the same step can be run again and then
-    matches the oracle.  The context stays usable throughout."""
-    wl = workload.custom(W=16, sizes=sizes, chunk=4096, keep_percent=25,
+    matches the oracle.  The context stays usable throughout.  With 16
+    workers in the shifted layout each tile is two stages (worker halves);
+    with 8, two CTAs share an SM."""
+    wl = workload.custom(W=W, sizes=sizes, chunk=4096, keep_percent=25,
                          config_id=220, steps=3)
     run = DeviceRun(wl, "pipeline", inplace=inplace)
     st = oracle.State(workload.initial_weights(wl))
