@@ -456,8 +456,8 @@ FC_API fc_status fc_step_noalloc(const void *const *grads, int32_t W,
 /* ---- test hook ------------------------------------------------------------------- */
 
 /* Exercises the failure path of the TMA-staged phase 1 (not part of the
- * method).  Arms the next TMA-staged launch (4, 8 or 16 workers on an
- * aligned layout) to issue no copies for fused tile `tile` (2048 elements),
+ * method).  Arms the next TMA-staged launch (4, 8 or 16 workers, aligned or
+ * shifted layout) to issue no copies for fused tile `tile` (2048 elements),
  * with every wait of that launch bounded by wait_limit_ns (1 ms .. 2 s)
  * instead of 2 s.  The waits on that tile then run out, the kernel records
  * the failure in the workspace and returns, and phase 2 reports it: the
