@@ -224,6 +224,9 @@ def test_reduce_kernel_choice_from_layout(fc_lib):
         fc.FC_REDUCE_REGISTER
     # worker counts, orders, chunk sizes and N the staged kernel does not serve
     assert k(separate(32, even), 256) == fc.FC_REDUCE_REGISTER
+    assert k(separate(32, odd), 256) == fc.FC_REDUCE_REGISTER
+    assert k(separate(64, [8192 * 2048]), 256) == fc.FC_REDUCE_REGISTER
+    assert k(separate(24, odd), 256) == fc.FC_REDUCE_REGISTER
     assert k(separate(2, even), 256) == fc.FC_REDUCE_REGISTER
     assert k(separate(8, even), 256, fc.FC_ORDER_SEQUENTIAL) == fc.FC_REDUCE_REGISTER
     assert k(separate(8, even), 256, fc.FC_ORDER_RING) == fc.FC_REDUCE_REGISTER
